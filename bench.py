@@ -1,0 +1,533 @@
+#!/usr/bin/env python
+"""Benchmark: GatedDeltaNet record + replay tokens/s and achieved HBM GB/s.
+
+One step = the whole hot path over one batch of the workload: the record
+kernel (T steps, delta tape plus k_log / g_log capture) followed by the
+replay kernel (the accepted prefix folded onto the pre-record snapshot).
+The default workload is the 128-sequence rollback case (B=128, T=16,
+Hk=16, Hv=32, Dk=Dv=128, bf16 inputs and tape, f32 state, Bernoulli(0.8)
+mask, accepted=11); ``--config`` picks another named workload.
+
+Timing: W untimed warm-up steps, then K steps between CUDA events on the
+launching stream, bracketed by a barrier and torch.cuda.synchronize(); with
+N processes (torchrun) every rank runs its own full batch (weak scaling, no
+data-path collective) and the maximum time over ranks is used.  The state
+buffers (256 MiB each at the default size) are larger than L2, so no flush
+is needed between steps.  Per-kernel durations come from event pairs around
+each launch inside the timed region.
+
+``--impl reference`` times the float64 CPU oracle on the same workload (a
+bounded batch sample per step) and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "GDN record+replay tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+DEFAULT_CONFIG = "rollback_b128_t16_bf16"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = os.path.join(ROOT, "linear_attention_recurrence_step_gb300", "csrc")
+
+
+# ---------------------------------------------------------------- accounting
+def algorithmic_bytes(case, accepted: int, capture: bool = True):
+    """Bytes the method must move (each touched once), per launch.
+
+    Record: the state read and written once (f32), plus for every active
+    (b, t): the q and k rows of its key head, the v row, g and beta, the y and
+    delta_log rows written (and k_log / g_log when captured), plus the mask.
+    Replay: the state read and written once, plus for every active (b, t) with
+    t < accepted: the delta_log row, the k_log row and g_log, plus the mask
+    entries it reads.  Masked-off and unaccepted steps move nothing."""
+    eb = workloads.elem_size(case.dtype)
+    B, T, Hk, Hv, Dk, Dv = case.B, case.T, case.Hk, case.Hv, case.Dk, case.Dv
+    act = np.ones((B, T), bool) if case.mask is None else case.mask.astype(bool)
+    n_act = int(act.sum())
+    state = B * Hv * Dv * Dk * 4
+    mask_b = 0 if case.mask is None else B * T * 4
+    per_step_rec = (2 * Hk * Dk + Hv * Dv + 2 * Hv + 2 * Hv * Dv) * eb
+    if capture:
+        per_step_rec += (Hv * Dk + Hv) * eb
+    rec = 2 * state + n_act * per_step_rec + mask_b
+    steps = min(accepted, T)
+    n_rep = int(act[:, :steps].sum())
+    rep = 2 * state + n_rep * (Hv * Dv + Hv * Dk + Hv) * eb + \
+        (0 if case.mask is None else B * steps * 4)
+    return rec, rep
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(KERNEL_SOURCES, "*"))):
+        if p.endswith((".cu", ".cuh", ".h")):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    entry = t.get("kernels", {}).get(f"{kernel}:{workload}")
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def _dist_init(world):
+    import torch
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x: float, dist, device=None) -> float:
+    """Max of a scalar over ranks (timing only: not part of the data path)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch (independent shard of the job)."""
+    return base_seed + 7919 * rank
+
+
+def _make_rank_case(config: str, rank: int):
+    spec = dict(workloads.CONFIGS[config])
+    seed = rank_seed(spec.pop("seed"), rank)
+    spec.pop("repeat", None)
+    return workloads.make_case(seed=seed, name=config, **spec)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import linear_attention_recurrence_step_gb300 as gdn
+
+    dist = _dist_init(world)
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = gdn.load()
+    case = _make_rank_case(args.config, rank)
+    uses_repeat = workloads.uses_repeat(args.config)
+    dt = case.dtype
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dt]
+    code = gdn.DTYPE_CODES[tdt]
+    B, T, Hk, Hv, Dk, Dv = case.B, case.T, case.Hk, case.Hv, case.Dk, case.Dv
+    acc = case.accepted
+
+    def host(arr):
+        if arr.dtype == np.uint16:
+            return torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16)
+        if arr.dtype == np.uint32:
+            return torch.from_numpy(arr.astype(np.int32))
+        return torch.from_numpy(np.ascontiguousarray(arr))
+
+    names = ["q", "k", "v", "g", "beta"]
+    h_in = {n: host(getattr(case, n)).pin_memory() for n in names}
+    h_in["state"] = host(case.state).pin_memory()
+    if case.mask is not None:
+        h_in["mask"] = host(case.mask).pin_memory()
+    d_in = {n: t.to(dev) for n, t in h_in.items()}
+    Hk_rec = Hv if uses_repeat else Hk
+    if uses_repeat:
+        d_in["qx"] = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
+        d_in["kx"] = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
+    y = torch.empty((B, T, Hv, Dv), dtype=tdt, device=dev)
+    dl = torch.empty_like(y)
+    kl = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
+    gl = torch.empty((B, T, Hv), dtype=tdt, device=dev)
+    s_rec = torch.empty_like(d_in["state"])
+    s_rep = torch.empty_like(d_in["state"])
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    mask_p = d_in["mask"].data_ptr() if "mask" in d_in else None
+    q_p = (d_in["qx"] if uses_repeat else d_in["q"]).data_ptr()
+    k_p = (d_in["kx"] if uses_repeat else d_in["k"]).data_ptr()
+    rec_args = (q_p, k_p, d_in["v"].data_ptr(), d_in["g"].data_ptr(), d_in["beta"].data_ptr(),
+                d_in["state"].data_ptr(), mask_p, y.data_ptr(), s_rec.data_ptr(), dl.data_ptr(),
+                kl.data_ptr(), gl.data_ptr(), B, T, Hk_rec, Hv, Dk, Dv, code, sp)
+    rep_args = (dl.data_ptr(), kl.data_ptr(), gl.data_ptr(), d_in["state"].data_ptr(), mask_p,
+                s_rep.data_ptr(), B, T, Hv, Dk, Dv, acc, code, sp)
+    eb = workloads.elem_size(dt)
+    rpt_q = (d_in["q"].data_ptr(), d_in["qx"].data_ptr() if uses_repeat else 0, B * T, Hk, Hv, Dk,
+             code, B * T * Hk * Dk * eb, B * T * Hv * Dk * eb, sp)
+    rpt_k = (d_in["k"].data_ptr(), d_in["kx"].data_ptr() if uses_repeat else 0, B * T, Hk, Hv, Dk,
+             code, B * T * Hk * Dk * eb, B * T * Hv * Dk * eb, sp)
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {gdn.STATUS_NAMES.get(st)}: {lib.gdn_last_error().decode()}")
+
+    def step(ev=None):
+        if uses_repeat:
+            check(lib.gqa_repeat_tiled(*rpt_q), "repeat q")
+            check(lib.gqa_repeat_tiled(*rpt_k), "repeat k")
+        if ev is not None:
+            ev[0].record(stream)
+        check(lib.gdn_step_record(*rec_args), "record")
+        if ev is not None:
+            ev[1].record(stream)
+        check(lib.gdn_state_replay(*rep_args), "replay")
+        if ev is not None:
+            ev[2].record(stream)
+
+    launches_per_step = 2 + (2 if uses_repeat else 0)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id if rank == 0 else None) as clocks:
+        t0.record(stream)
+        for i in range(K):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    rec_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in evs)
+    rep_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in evs)
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
+
+    tokens_per_step = B * T
+    ms_per_step = elapsed_ms / K
+    value = world * tokens_per_step * K / (elapsed_ms / 1e3)
+    rec_b, rep_b = algorithmic_bytes(case, acc, capture=True)
+    peak, peak_src = hbm_peak()
+    rec_gbs = rec_b / (rec_ms * 1e-3) / 1e9
+    rep_gbs = rep_b / (rep_ms * 1e-3) / 1e9
+    step_bytes = rec_b + rep_b
+    if uses_repeat:
+        step_bytes += 2 * (B * T * Hk * Dk + B * T * Hv * Dk) * eb
+    step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers (pinned): H2D of the
+    # step's inputs, both kernels, D2H of y, the tape and the replayed state.
+    e2e_steps = max(1, min(args.e2e_steps, K))
+    h_y = torch.empty(y.shape, dtype=tdt).pin_memory()
+    h_dl = torch.empty(dl.shape, dtype=tdt).pin_memory()
+    h_st = torch.empty(s_rep.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in (h_y, h_dl, h_st))
+
+    def e2e_step():
+        for n, t in h_in.items():
+            d_in[n].copy_(t, non_blocking=True)
+        step()
+        h_y.copy_(y, non_blocking=True)
+        h_dl.copy_(dl, non_blocking=True)
+        h_st.copy_(s_rep, non_blocking=True)
+
+    for _ in range(min(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_value = world * tokens_per_step * e2e_steps / (e2e_ms / 1e3)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    dominant = "record" if rec_ms >= rep_ms else "replay"
+    dom_ms = rec_ms if dominant == "record" else rep_ms
+    dom_b = rec_b if dominant == "record" else rep_b
+    achieved = dom_b / (dom_ms * 1e-3) / 1e9
+    traffic = measured_traffic(dominant, args.config)
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": args.config, "B": B, "T": T, "Hk": Hk, "Hv": Hv, "Dk": Dk, "Dv": Dv,
+            "io_dtype": dt, "state_dtype": "f32", "accepted": acc,
+            "mask": workloads.CONFIGS[args.config]["mask"],
+            "tape_capture": "delta_log+k_log+g_log",
+            "l2": f"inputs larger than L2 (state {B * Hv * Dv * Dk * 4 >> 20} MiB per buffer)",
+            "parallelism": f"{world} independent batch shard(s), no collective",
+        },
+        "hbm_gbs_step": step_gbs,
+        "hbm_frac_step": step_gbs / peak,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": dom_b, "peak_source": peak_src},
+        "kernels": {
+            "record": {"us": rec_ms * 1e3, "algorithmic_bytes": rec_b, "gbs": rec_gbs,
+                       "frac": rec_gbs / peak},
+            "replay": {"us": rep_ms * 1e3, "algorithmic_bytes": rep_b, "gbs": rep_gbs,
+                       "frac": rep_gbs / peak},
+        },
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return out
+
+
+# ---------------------------------------------------------------- oracle legs
+def _oracle_inputs(orc, case, bs: int):
+    """Float64 inputs of the first ``bs`` sequences (q / k expanded when the
+    workload uses the tiled repeat; that expansion is part of the timed work)."""
+    sl = slice(0, bs)
+    return dict(q=case.f64("q")[sl].copy(), k=case.f64("k")[sl].copy(),
+                v=case.f64("v")[sl].copy(), g=case.f64("g")[sl].copy(),
+                beta=case.f64("beta")[sl].copy(), state=case.f64("state")[sl].copy(),
+                mask=None if case.mask is None else case.mask[sl].copy())
+
+
+def _oracle_step(orc, case, inp):
+    """One oracle record + replay on prepared float64 inputs."""
+    q, k = inp["q"], inp["k"]
+    if workloads.uses_repeat(case.name):
+        Bs = q.shape[0]
+        q = orc.repeat_tiled(q.reshape(Bs * case.T, case.Hk, case.Dk), case.Hv).reshape(
+            Bs, case.T, case.Hv, case.Dk)
+        k = orc.repeat_tiled(k.reshape(Bs * case.T, case.Hk, case.Dk), case.Hv).reshape(
+            Bs, case.T, case.Hv, case.Dk)
+    rec = orc.record(q, k, inp["v"], inp["g"], inp["beta"], inp["state"], inp["mask"])
+    orc.replay(rec["delta_log"], rec["k_log"], rec["g_log"], inp["state"], inp["mask"],
+               accepted=case.accepted)
+
+
+def cpu_baseline(case, seconds: float):
+    """The float64 oracle, as it stands, on the host cores: whole-batch record
+    + replay repeated for about ``seconds``; tokens/s."""
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    inp = _oracle_inputs(oracle, case, case.B)
+    t_start = time.perf_counter()
+    reps = 0
+    while True:
+        _oracle_step(oracle, case, inp)
+        reps += 1
+        el = time.perf_counter() - t_start
+        if el >= seconds or reps >= 1000:
+            break
+    return {"value": reps * case.B * case.T / el, "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{reps} x full batch (B={case.B}, T={case.T}) record+replay, "
+                      f"{el:.1f} s, float64, OpenMP over (b, hv)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    case = workloads.make_config(args.config)
+    threads = oracle.max_threads()
+    # size the per-step batch sample so the whole run stays within ~2 minutes
+    one = _oracle_inputs(oracle, case, 1)
+    t = time.perf_counter()
+    _oracle_step(oracle, case, one)
+    t1 = time.perf_counter() - t
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    bs = int(max(1, min(case.B, budget / max(t1, 1e-6))))
+    inp = _oracle_inputs(oracle, case, bs)
+    for i in range(args.warmup):
+        _oracle_step(oracle, case, inp)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_step(oracle, case, inp)
+    el = time.perf_counter() - t
+    value = args.steps * bs * case.T / el
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.config, "B": case.B, "T": case.T, "Hk": case.Hk,
+                   "Hv": case.Hv, "Dk": case.Dk, "Dv": case.Dv, "io_dtype": case.dtype,
+                   "accepted": case.accepted, "batch_sample_per_step": bs},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{bs} of {case.B} sequences per step, record+replay, "
+                                   "float64 oracle, OpenMP over (b, hv)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return out
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", choices=sorted(workloads.CONFIGS), default=DEFAULT_CONFIG)
+    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if args.steps < 1:
+        p.error("--steps must be >= 1")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and "WORLD_SIZE" in os.environ:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}; using WORLD_SIZE",
+              file=sys.stderr)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local_rank)
+    if out is not None:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

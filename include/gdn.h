@@ -1,0 +1,169 @@
+/*
+ * gdn.h -- C ABI of the GB300 GatedDeltaNet record / replay library (libgdn.so).
+ *
+ * The library runs the gated delta-rule recurrence step with innovation-tape
+ * capture ("record"), the speculative-decode rollback that re-folds an
+ * accepted tape prefix onto a state snapshot ("replay"), and the tiled GQA
+ * head broadcast ("repeat"), as hand-written sm_103a CUDA kernels.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a pointer to caller-owned, densely packed,
+ *   row-major DEVICE memory (any pointer the CUDA runtime can dereference
+ *   from a kernel).  The library never allocates, frees, copies to the host
+ *   or synchronises: it validates its arguments on the host, enqueues one
+ *   kernel on `stream` and returns.  Results are ready when the stream has
+ *   reached that point.
+ * - `stream` is a cudaStream_t (the typedef below is the same type);
+ *   NULL means the legacy default stream.
+ * - Dimensions are int64_t and must be > 0 (a zero or negative dimension is
+ *   GDN_ERR_INVALID_ARGUMENT, the rule the tiled-repeat page applies to its
+ *   own shapes).
+ * - Validation happens before any launch.  A non-GDN_OK status means nothing
+ *   was enqueued, except GDN_ERR_CUDA, which reports a failed launch.
+ *   gdn_last_error() returns a message for the last failure on the calling
+ *   host thread.
+ * - Floating-point tensors share one element type `dtype` (f32, bf16 or
+ *   f16); the recurrent state is always float32.  All arithmetic is float32;
+ *   values written in bf16/f16 are rounded to nearest-even.
+ *
+ * Notation: B batch, T timesteps, Hk key heads, Hv value heads (Hv % Hk == 0,
+ * G = Hv / Hk, key head of value head hv is hk = hv / G), Dk key dim, Dv
+ * value dim.  The source page for record and replay is "metaltile-std 0.1.0
+ * -- src/ffai/gated_delta_replay.rs" (module doc, kernels
+ * gated_delta_step_record and state_replay); the source page for the repeat
+ * is "mlx-native 0.6.5 -- ops/repeat_tiled.rs" (module doc "Mapping",
+ * dispatch_repeat_tiled_f32).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARGUMENT = 1, /* bad shape, null pointer, overflow, overlap  */
+    GDN_ERR_UNSUPPORTED = 2,      /* dtype or Dk outside the compiled set        */
+    GDN_ERR_MISALIGNED = 3,       /* a pointer breaks its alignment requirement  */
+    GDN_ERR_CUDA = 4              /* the CUDA runtime rejected the launch        */
+} gdn_status;
+
+typedef enum gdn_dtype {
+    GDN_DTYPE_F32 = 0,
+    GDN_DTYPE_BF16 = 1,
+    GDN_DTYPE_F16 = 2
+} gdn_dtype;
+
+/*
+ * gdn_step_record -- T recurrence steps with delta-tape capture
+ * (page: gated_delta_step_record; tape layout: module doc).
+ *
+ * For every state row s = state[b,hv,dv,:] (float32, Dk entries) and every
+ * step t in 0..T-1 whose mask is on:
+ *     s        <- g[b,t,hv] * s
+ *     kv        = s . k[b,t,hk,:]
+ *     delta     = (v[b,t,hv,dv] - kv) * beta[b,t,hv]
+ *     delta_log[b,t,hv,dv] = delta
+ *     s        <- s + k[b,t,hk,:] * delta
+ *     y[b,t,hv,dv] = s . q[b,t,hk,:]
+ * and state_out[b,hv,dv,:] = s after the last step.
+ *
+ * Arguments (shape, element type, alignment):
+ *   q, k       [B,T,Hk,Dk]  dtype, 16-byte aligned
+ *   v          [B,T,Hv,Dv]  dtype
+ *   g, beta    [B,T,Hv]     dtype (g is a multiplicative decay, not a log)
+ *   state_in   [B,Hv,Dv,Dk] float32, 16-byte aligned (the snapshot)
+ *   mask       [B,T] uint32 or NULL.  NULL: every step is on.  A step with
+ *              mask 0 is skipped: the state is unchanged and y, delta_log,
+ *              k_log, g_log at (b,t) are NOT written (they keep whatever the
+ *              caller put there).  Any nonzero value means on.
+ *   y          [B,T,Hv,Dv]  dtype (output)
+ *   state_out  [B,Hv,Dv,Dk] float32, 16-byte aligned (output).  May be the
+ *              same pointer as state_in (in place); any other overlap with
+ *              state_in is GDN_ERR_INVALID_ARGUMENT.
+ *   delta_log  [B,T,Hv,Dv]  dtype (output, the innovation tape)
+ *   k_log      [B,T,Hv,Dk]  dtype or NULL (output): k expanded to value heads,
+ *              k_log[b,t,hv,:] = k[b,t,hv/G,:], written where delta_log is
+ *   g_log      [B,T,Hv]     dtype or NULL (output): copy of g, written where
+ *              delta_log is
+ *   Dk         32, 64, 128, 192 or 256 (else GDN_ERR_UNSUPPORTED); Dv any > 0
+ * Outputs must not overlap inputs (other than the in-place state).
+ */
+gdn_status gdn_step_record(const void *q, const void *k, const void *v,
+                           const void *g, const void *beta,
+                           const float *state_in, const uint32_t *mask,
+                           void *y, float *state_out, void *delta_log,
+                           void *k_log, void *g_log,
+                           int64_t B, int64_t T, int64_t Hk, int64_t Hv,
+                           int64_t Dk, int64_t Dv, gdn_dtype dtype,
+                           gdn_stream_t stream);
+
+/*
+ * gdn_state_replay -- rebuild the state after an accepted prefix of the tape
+ * (page: state_replay; module doc: "re-folds the accepted prefix").
+ *
+ * For every state row and t in 0..T-1:
+ *     do_step = (t < accepted) && (mask == NULL || mask[b,t] != 0)
+ *     s <- do_step ? s * g_log[b,t,hv] + k_log[b,t,hv,:] * delta_log[b,t,hv,dv] : s
+ * The select is a true select: tape slots of skipped steps are never read,
+ * so they may hold anything (NaN, stale data).
+ *
+ *   delta_log  [B,T,Hv,Dv]  dtype
+ *   k_log      [B,T,Hv,Dk]  dtype, 16-byte aligned (key rows expanded to value heads)
+ *   g_log      [B,T,Hv]     dtype
+ *   state_in   [B,Hv,Dv,Dk] float32, 16-byte aligned (the pre-record snapshot)
+ *   mask       [B,T] uint32 or NULL (the mask record was given)
+ *   state_out  [B,Hv,Dv,Dk] float32, 16-byte aligned; may equal state_in
+ *   accepted   >= 0; values above T act as T; 0 copies state_in to state_out
+ *
+ * With a float32 tape written by gdn_step_record from the same snapshot and
+ * mask, replay with accepted >= T reproduces record's state_out bit for bit,
+ * and replay with accepted = a reproduces a record over the first a steps.
+ */
+gdn_status gdn_state_replay(const void *delta_log, const void *k_log,
+                            const void *g_log, const float *state_in,
+                            const uint32_t *mask, float *state_out,
+                            int64_t B, int64_t T, int64_t Hv, int64_t Dk,
+                            int64_t Dv, int64_t accepted, gdn_dtype dtype,
+                            gdn_stream_t stream);
+
+/*
+ * gqa_repeat_tiled -- tiled GQA broadcast (page: repeat_tiled.rs, "Mapping"):
+ *     dst[t, hh, x] = src[t, hh % hg, x],  src [seq,hg,k] -> dst [seq,h,k]
+ * A bit-exact copy.  Errors follow dispatch_repeat_tiled_f32: any dimension
+ * <= 0, h % hg != 0, an element count or byte size that overflows, or
+ * src_bytes / dst_bytes smaller than the shapes need ->
+ * GDN_ERR_INVALID_ARGUMENT.  Any dtype of the enum is accepted; pointers
+ * need only the element alignment (16-byte alignment with k * elemsize a
+ * multiple of 16 takes the vector path).  src and dst must not overlap.
+ */
+gdn_status gqa_repeat_tiled(const void *src, void *dst,
+                            int64_t seq, int64_t hg, int64_t h, int64_t k,
+                            gdn_dtype dtype, size_t src_bytes, size_t dst_bytes,
+                            gdn_stream_t stream);
+
+/* Static name of a status code ("GDN_OK", ...); never NULL. */
+const char *gdn_status_string(gdn_status status);
+
+/* Message for the last non-OK status returned on the calling host thread
+ * ("" if none).  Valid until the next call from the same thread. */
+const char *gdn_last_error(void);
+
+/* GDN_ABI_VERSION of the loaded library. */
+int gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,213 @@
+"""GB300 GatedDeltaNet record / replay with innovation-tape capture.
+
+A thin ctypes binding over ``libgdn.so`` (C ABI: ``include/gdn.h``).  The
+functions below only check tensor metadata, allocate missing outputs with
+PyTorch and forward raw device pointers plus the current CUDA stream; every
+step of the computation runs in the library's sm_103a kernels.  There is no
+CPU or PyTorch fallback: if the library has not been built (``build()``) or
+cannot be loaded, every call raises ``GdnError``.
+
+Entry points (same names as the C ABI):
+
+* ``gdn_step_record`` -- T gated delta-rule steps; writes y, the final state
+  and the delta tape (optionally k_log / g_log), "metaltile-std
+  gated_delta_replay.rs", kernel gated_delta_step_record.
+* ``gdn_state_replay`` -- re-fold the accepted tape prefix onto a snapshot,
+  same page, kernel state_replay.
+* ``gqa_repeat_tiled`` -- ``dst[t,h,k] = src[t,h%hg,k]``, "mlx-native
+  repeat_tiled.rs".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from collections import namedtuple
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = ["GdnError", "build", "load", "lib_path", "gdn_step_record", "gdn_state_replay",
+           "gqa_repeat_tiled", "RecordOutputs", "STATUS_NAMES", "DTYPE_CODES"]
+
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPORTED",
+                3: "GDN_ERR_MISALIGNED", 4: "GDN_ERR_CUDA"}
+DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+EXPORTED = ("gdn_step_record", "gdn_state_replay", "gqa_repeat_tiled", "gdn_status_string",
+            "gdn_last_error", "gdn_abi_version")
+
+RecordOutputs = namedtuple("RecordOutputs", "y state_out delta_log k_log g_log")
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+
+
+class GdnError(RuntimeError):
+    """A non-OK status from libgdn.so, or the library is missing."""
+
+    def __init__(self, msg: str, status: int = -1):
+        super().__init__(msg)
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    """Compile libgdn.so for sm_103a (in-tree) and return its path."""
+    return _build.build(force=force)
+
+
+def _declare(lib: ctypes.CDLL) -> None:
+    lib.gdn_step_record.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int, _P]
+    lib.gdn_step_record.restype = ctypes.c_int
+    lib.gdn_state_replay.argtypes = [_P] * 6 + [_I] * 6 + [ctypes.c_int, _P]
+    lib.gdn_state_replay.restype = ctypes.c_int
+    lib.gqa_repeat_tiled.argtypes = [_P, _P] + [_I] * 4 + [ctypes.c_int, ctypes.c_size_t,
+                                                            ctypes.c_size_t, _P]
+    lib.gqa_repeat_tiled.restype = ctypes.c_int
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_last_error.argtypes = []
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_abi_version.argtypes = []
+    lib.gdn_abi_version.restype = ctypes.c_int
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libgdn.so (raises GdnError if it is missing: no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or lib_path()
+        if not os.path.exists(p):
+            raise GdnError(f"libgdn.so not found at {p}; build it first "
+                           "(linear_attention_recurrence_step_gb300.build())")
+        lib = ctypes.CDLL(p)
+        _declare(lib)
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        lib = load()
+        msg = lib.gdn_last_error().decode(errors="replace")
+        raise GdnError(f"{what}: {STATUS_NAMES.get(status, status)}: {msg}", status)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, shape, dtype, device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def gdn_step_record(q, k, v, g, beta, state_in, mask=None, *, y=None, state_out=None,
+                    delta_log=None, k_log=None, g_log=None, capture_tape: bool = False,
+                    stream=None) -> RecordOutputs:
+    """Run T record steps.  Missing outputs are allocated (uninitialised where
+    the mask skips a step).  ``capture_tape=True`` also allocates k_log/g_log.
+    ``state_out=state_in`` runs in place."""
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dt, dev = q.dtype, q.device
+    if dt not in DTYPE_CODES:
+        raise ValueError(f"unsupported dtype {dt}")
+    _need(q, "q", (B, T, Hk, Dk), dt, dev)
+    _need(k, "k", (B, T, Hk, Dk), dt, dev)
+    _need(v, "v", (B, T, Hv, Dv), dt, dev)
+    _need(g, "g", (B, T, Hv), dt, dev)
+    _need(beta, "beta", (B, T, Hv), dt, dev)
+    _need(state_in, "state_in", (B, Hv, Dv, Dk), torch.float32, dev)
+    if mask is not None:
+        _need(mask, "mask", (B, T), torch.int32 if mask.dtype == torch.int32 else torch.uint32, dev)
+    if y is None:
+        y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    if delta_log is None:
+        delta_log = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    if capture_tape:
+        if k_log is None:
+            k_log = torch.empty((B, T, Hv, Dk), dtype=dt, device=dev)
+        if g_log is None:
+            g_log = torch.empty((B, T, Hv), dtype=dt, device=dev)
+    _need(y, "y", (B, T, Hv, Dv), dt, dev)
+    _need(state_out, "state_out", (B, Hv, Dv, Dk), torch.float32, dev)
+    _need(delta_log, "delta_log", (B, T, Hv, Dv), dt, dev)
+    if k_log is not None:
+        _need(k_log, "k_log", (B, T, Hv, Dk), dt, dev)
+    if g_log is not None:
+        _need(g_log, "g_log", (B, T, Hv), dt, dev)
+    st = load().gdn_step_record(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(mask), _ptr(y),
+        _ptr(state_out), _ptr(delta_log), _ptr(k_log), _ptr(g_log), B, T, Hk, Hv, Dk, Dv,
+        DTYPE_CODES[dt], _stream(dev, stream))
+    _check(st, "gdn_step_record")
+    return RecordOutputs(y, state_out, delta_log, k_log, g_log)
+
+
+def gdn_state_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted: int,
+                     state_out=None, stream=None) -> torch.Tensor:
+    """Fold the tape prefix [0, accepted) onto ``state_in``; returns state_out."""
+    B, T, Hv, Dv = delta_log.shape
+    Dk = k_log.shape[3]
+    dt, dev = delta_log.dtype, delta_log.device
+    if dt not in DTYPE_CODES:
+        raise ValueError(f"unsupported dtype {dt}")
+    _need(delta_log, "delta_log", (B, T, Hv, Dv), dt, dev)
+    _need(k_log, "k_log", (B, T, Hv, Dk), dt, dev)
+    _need(g_log, "g_log", (B, T, Hv), dt, dev)
+    _need(state_in, "state_in", (B, Hv, Dv, Dk), torch.float32, dev)
+    if mask is not None:
+        _need(mask, "mask", (B, T), torch.int32 if mask.dtype == torch.int32 else torch.uint32, dev)
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    _need(state_out, "state_out", (B, Hv, Dv, Dk), torch.float32, dev)
+    st = load().gdn_state_replay(
+        _ptr(delta_log), _ptr(k_log), _ptr(g_log), _ptr(state_in), _ptr(mask), _ptr(state_out),
+        B, T, Hv, Dk, Dv, int(accepted), DTYPE_CODES[dt], _stream(dev, stream))
+    _check(st, "gdn_state_replay")
+    return state_out
+
+
+def gqa_repeat_tiled(src, h: int, *, dst=None, stream=None) -> torch.Tensor:
+    """Tiled GQA broadcast ``[seq,hg,k] -> [seq,h,k]``, ``dst[t,hh,x] = src[t,hh%hg,x]``."""
+    seq, hg, kd = src.shape
+    dt, dev = src.dtype, src.device
+    if dt not in DTYPE_CODES:
+        raise ValueError(f"unsupported dtype {dt}")
+    if not src.is_contiguous():
+        raise ValueError("src must be contiguous")
+    if dst is None:
+        dst = torch.empty((seq, h, kd), dtype=dt, device=dev)
+    _need(dst, "dst", (seq, h, kd), dt, dev)
+    st = load().gqa_repeat_tiled(_ptr(src), _ptr(dst), seq, hg, h, kd, DTYPE_CODES[dt],
+                                 src.numel() * src.element_size(),
+                                 dst.numel() * dst.element_size(), _stream(dev, stream))
+    _check(st, "gqa_repeat_tiled")
+    return dst

@@ -1,0 +1,294 @@
+// abi.cu -- the C ABI of libgdn.so (declared in include/gdn.h): argument
+// validation, launch geometry and dispatch.  Validation happens entirely on
+// the host, before any CUDA call, and follows the error rules of
+// dispatch_repeat_tiled_f32 ("mlx-native repeat_tiled.rs"): zero dimensions,
+// a head count that does not divide, size products that overflow and buffers
+// that are too small are invalid arguments.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "gdn.h"
+#include "launch.h"
+#include "record.cuh"
+#include "replay.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gdn_status fail(gdn_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+gdn_status ok() {
+    g_last_error.clear();
+    return GDN_OK;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_mul_overflow(a, b, out); }
+
+// Product of dims (all > 0) times elem_bytes, or -1 on overflow.
+int64_t nbytes(std::initializer_list<int64_t> dims, int64_t elem_bytes) {
+    int64_t acc = elem_bytes;
+    for (int64_t d : dims)
+        if (!mul_ok(acc, d, &acc)) return -1;
+    return acc;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void *a, int64_t na, const void *b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+int elem_bytes(gdn_dtype dt) {
+    switch (dt) {
+    case GDN_DTYPE_F32: return 4;
+    case GDN_DTYPE_BF16: return 2;
+    case GDN_DTYPE_F16: return 2;
+    }
+    return 0;
+}
+
+gdn_status cuda_fail(const char *what, cudaError_t e) {
+    return fail(GDN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// SM count of the current device (0 if it cannot be read).
+int current_sm_count(cudaError_t *err) {
+    int dev = 0, sms = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return 0;
+    *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+namespace gdn {
+
+bool supported_dk(int64_t dk) {
+    return dk == 32 || dk == 64 || dk == 128 || dk == 192 || dk == 256;
+}
+
+int rows_per_warp(int dk) {
+    switch (dk) {
+    case 32: return TileLayout<32>::RW;
+    case 64: return TileLayout<64>::RW;
+    case 128: return TileLayout<128>::RW;
+    case 192: return TileLayout<192>::RW;
+    case 256: return TileLayout<256>::RW;
+    }
+    return 0;
+}
+
+// Warps per CTA: a whole tile's rows when the grid still covers every SM
+// twice, fewer (rows of a tile split over several CTAs) when tiles are few.
+static int pick_warps(int rw, int64_t tiles, int64_t Dv, int sm_count) {
+    int nw = (int)std::min<int64_t>(TileLayout<128>::MAX_WARPS, ceil_div(Dv, rw));
+    const int64_t want = 2 * (int64_t)(sm_count > 0 ? sm_count : 1);
+    while (nw > 1 && tiles * ceil_div(Dv, (int64_t)nw * rw) < want) nw = (nw + 1) / 2;
+    return nw;
+}
+
+static constexpr int kChunk = 16;  // timesteps staged in shared memory at a time
+
+Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int sm_count) {
+    const int rw = rows_per_warp(dk);
+    const int nw = pick_warps(rw, tiles, Dv, sm_count);
+    Geometry g;
+    g.threads = 32 * nw;
+    g.rows_cta = nw * rw;
+    g.row_blocks = ceil_div(Dv, g.rows_cta);
+    g.tc = (int)std::min<int64_t>(T, kChunk);
+    g.smem = record_smem_bytes(dk, g.tc, g.rows_cta);
+    return g;
+}
+
+Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int sm_count) {
+    const int rw = rows_per_warp(dk);
+    const int nw = pick_warps(rw, tiles, Dv, sm_count);
+    Geometry g;
+    g.threads = 32 * nw;
+    g.rows_cta = nw * rw;
+    g.row_blocks = ceil_div(Dv, g.rows_cta);
+    g.tc = (int)std::max<int64_t>(1, std::min<int64_t>(steps, kChunk));
+    g.smem = replay_smem_bytes(dk, g.tc, g.rows_cta);
+    return g;
+}
+
+}  // namespace gdn
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status status) {
+    switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARGUMENT: return "GDN_ERR_INVALID_ARGUMENT";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+const char *gdn_last_error(void) { return g_last_error.c_str(); }
+
+int gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+gdn_status gdn_step_record(const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, const float *state_in, const uint32_t *mask,
+                           void *y, float *state_out, void *delta_log, void *k_log, void *g_log,
+                           int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                           gdn_dtype dtype, gdn_stream_t stream) {
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "gdn_step_record: unknown dtype %d", (int)dtype);
+    if (B <= 0 || T <= 0 || Hk <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "gdn_step_record: B, T, Hk, Hv, Dk, Dv must all be > 0 (got %lld %lld %lld %lld %lld %lld)",
+                    (long long)B, (long long)T, (long long)Hk, (long long)Hv, (long long)Dk, (long long)Dv);
+    if (Hv % Hk != 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: Hv (%lld) must be a multiple of Hk (%lld)",
+                    (long long)Hv, (long long)Hk);
+    if (!q || !k || !v || !g || !beta || !state_in || !y || !state_out || !delta_log)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "gdn_step_record: q, k, v, g, beta, state_in, y, state_out, delta_log must be non-NULL");
+    if (Dk % 32 != 0 || !gdn::supported_dk(Dk))
+        return fail(GDN_ERR_UNSUPPORTED, "gdn_step_record: Dk = %lld not supported (32, 64, 128, 192, 256)",
+                    (long long)Dk);
+    const int64_t qk_b = nbytes({B, T, Hk, Dk}, eb), v_b = nbytes({B, T, Hv, Dv}, eb);
+    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), kl_b = nbytes({B, T, Hv, Dk}, eb);
+    const int64_t gb_b = nbytes({B, T, Hv}, eb), m_b = nbytes({B, T}, 4);
+    int64_t blocks_bound = 0;
+    if (qk_b < 0 || v_b < 0 || s_b < 0 || kl_b < 0 || gb_b < 0 || m_b < 0 ||
+        !mul_ok(B * Hv, Dv, &blocks_bound))
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: tensor sizes overflow int64");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(state_in, 16) || !aligned(state_out, 16))
+        return fail(GDN_ERR_MISALIGNED, "gdn_step_record: q, k, state_in, state_out must be 16-byte aligned");
+    if (!aligned(v, eb) || !aligned(g, eb) || !aligned(beta, eb) || !aligned(y, eb) ||
+        !aligned(delta_log, eb) || !aligned(k_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4))
+        return fail(GDN_ERR_MISALIGNED, "gdn_step_record: a tensor is not aligned to its element size");
+    if (state_in != state_out && overlap(state_in, s_b, state_out, s_b))
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "gdn_step_record: state_out overlaps state_in without being the same buffer");
+
+    cudaError_t e;
+    const int sms = current_sm_count(&e);
+    if (e != cudaSuccess) return cuda_fail("gdn_step_record: device query", e);
+    const gdn::Geometry geo = gdn::record_geometry((int)Dk, B * Hv, Dv, T, sms);
+    if ((B * Hv) > (int64_t)INT32_MAX / geo.row_blocks)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: grid too large (B*Hv*row_blocks > 2^31-1)");
+    gdn::RecordArgs a{q, k, v, g, beta, state_in, mask, y, state_out, delta_log, k_log, g_log,
+                      B, T, Hk, Hv, Dv, geo.rows_cta, geo.row_blocks, geo.tc};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (dtype) {
+    case GDN_DTYPE_F32: e = gdn::launch_record_f32((int)Dk, a, geo, s); break;
+    case GDN_DTYPE_BF16: e = gdn::launch_record_bf16((int)Dk, a, geo, s); break;
+    case GDN_DTYPE_F16: e = gdn::launch_record_f16((int)Dk, a, geo, s); break;
+    }
+    if (e != cudaSuccess) return cuda_fail("gdn_step_record: launch", e);
+    return ok();
+}
+
+gdn_status gdn_state_replay(const void *delta_log, const void *k_log, const void *g_log,
+                            const float *state_in, const uint32_t *mask, float *state_out,
+                            int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv,
+                            int64_t accepted, gdn_dtype dtype, gdn_stream_t stream) {
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "gdn_state_replay: unknown dtype %d", (int)dtype);
+    if (B <= 0 || T <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "gdn_state_replay: B, T, Hv, Dk, Dv must all be > 0 (got %lld %lld %lld %lld %lld)",
+                    (long long)B, (long long)T, (long long)Hv, (long long)Dk, (long long)Dv);
+    if (accepted < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay: accepted (%lld) must be >= 0",
+                    (long long)accepted);
+    if (!delta_log || !k_log || !g_log || !state_in || !state_out)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "gdn_state_replay: delta_log, k_log, g_log, state_in, state_out must be non-NULL");
+    if (Dk % 32 != 0 || !gdn::supported_dk(Dk))
+        return fail(GDN_ERR_UNSUPPORTED, "gdn_state_replay: Dk = %lld not supported (32, 64, 128, 192, 256)",
+                    (long long)Dk);
+    const int64_t d_b = nbytes({B, T, Hv, Dv}, eb), kl_b = nbytes({B, T, Hv, Dk}, eb);
+    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), g_b = nbytes({B, T, Hv}, eb);
+    const int64_t m_b = nbytes({B, T}, 4);
+    if (d_b < 0 || kl_b < 0 || s_b < 0 || g_b < 0 || m_b < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay: tensor sizes overflow int64");
+    if (!aligned(k_log, 16) || !aligned(state_in, 16) || !aligned(state_out, 16))
+        return fail(GDN_ERR_MISALIGNED, "gdn_state_replay: k_log, state_in, state_out must be 16-byte aligned");
+    if (!aligned(delta_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4))
+        return fail(GDN_ERR_MISALIGNED, "gdn_state_replay: a tensor is not aligned to its element size");
+    if (state_in != state_out && overlap(state_in, s_b, state_out, s_b))
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "gdn_state_replay: state_out overlaps state_in without being the same buffer");
+
+    const int64_t steps = accepted < T ? accepted : T;
+    if (steps == 0 && state_in == state_out) return ok();  // identity, nothing to do
+    cudaError_t e;
+    const int sms = current_sm_count(&e);
+    if (e != cudaSuccess) return cuda_fail("gdn_state_replay: device query", e);
+    const gdn::Geometry geo = gdn::replay_geometry((int)Dk, B * Hv, Dv, steps, sms);
+    if ((B * Hv) > (int64_t)INT32_MAX / geo.row_blocks)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay: grid too large");
+    gdn::ReplayArgs a{delta_log, k_log, g_log, state_in, mask, state_out, B, T, Hv, Dv, steps,
+                      geo.rows_cta, geo.row_blocks, geo.tc};
+    e = gdn::launch_replay(static_cast<gdn::DType>(dtype), (int)Dk, a, geo,
+                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("gdn_state_replay: launch", e);
+    return ok();
+}
+
+gdn_status gqa_repeat_tiled(const void *src, void *dst, int64_t seq, int64_t hg, int64_t h,
+                            int64_t k, gdn_dtype dtype, size_t src_bytes, size_t dst_bytes,
+                            gdn_stream_t stream) {
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "gqa_repeat_tiled: unknown dtype %d", (int)dtype);
+    if (seq <= 0 || hg <= 0 || h <= 0 || k <= 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: seq, hg, h, k must all be > 0");
+    if (h % hg != 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: h (%lld) must be a multiple of hg (%lld)",
+                    (long long)h, (long long)hg);
+    const int64_t need_src = nbytes({seq, hg, k}, eb);
+    if (need_src < 0) return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: seq*hg*k overflows");
+    const int64_t need_dst = nbytes({seq, h, k}, eb);
+    if (need_dst < 0) return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: seq*h*k overflows");
+    if (!src || !dst) return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: src and dst must be non-NULL");
+    if (src_bytes < (uint64_t)need_src)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: src buffer too small: need %lld bytes, have %llu",
+                    (long long)need_src, (unsigned long long)src_bytes);
+    if (dst_bytes < (uint64_t)need_dst)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: dst buffer too small: need %lld bytes, have %llu",
+                    (long long)need_dst, (unsigned long long)dst_bytes);
+    if (!aligned(src, eb) || !aligned(dst, eb))
+        return fail(GDN_ERR_MISALIGNED, "gqa_repeat_tiled: src / dst not aligned to the element size");
+    if (overlap(src, need_src, dst, need_dst))
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: src and dst overlap");
+
+    cudaError_t e;
+    const int sms = current_sm_count(&e);
+    if (e != cudaSuccess) return cuda_fail("gqa_repeat_tiled: device query", e);
+    gdn::RepeatArgs a;
+    a.src = src;
+    a.dst = dst;
+    a.seq = seq;
+    a.hg = hg;
+    a.h = h;
+    a.row_bytes = k * eb;
+    a.elem_bytes = eb;
+    a.vec16 = (a.row_bytes % 16 == 0) && aligned(src, 16) && aligned(dst, 16);
+    e = gdn::launch_repeat(a, reinterpret_cast<cudaStream_t>(stream), sms);
+    if (e != cudaSuccess) return cuda_fail("gqa_repeat_tiled: launch", e);
+    return ok();
+}
+
+}  // extern "C"

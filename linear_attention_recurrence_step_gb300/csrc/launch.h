@@ -1,0 +1,71 @@
+// launch.h -- internal interface between the C ABI (abi.cu) and the kernel
+// translation units.  Arguments arrive here already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+enum class DType : int { F32 = 0, BF16 = 1, F16 = 2 };
+
+// Launch geometry chosen on the host: each CTA owns `rows_cta` consecutive
+// value rows (dv) of one (b, hv) state tile; `row_blocks` CTAs cover a tile;
+// `tc` timesteps are staged in shared memory at a time.
+struct Geometry {
+    int threads;        // blockDim.x (a multiple of 32)
+    int rows_cta;       // value rows per CTA
+    int64_t row_blocks; // ceil(Dv / rows_cta)
+    int tc;             // staged chunk length in timesteps
+    size_t smem;        // dynamic shared memory bytes
+};
+
+struct RecordArgs {
+    const void *q, *k, *v, *g, *beta;
+    const float *state_in;
+    const uint32_t *mask;
+    void *y;
+    float *state_out;
+    void *delta_log, *k_log, *g_log;
+    int64_t B, T, Hk, Hv, Dv;
+    int rows_cta;
+    int64_t row_blocks;
+    int tc;
+};
+
+struct ReplayArgs {
+    const void *delta_log, *k_log, *g_log;
+    const float *state_in;
+    const uint32_t *mask;
+    float *state_out;
+    int64_t B, T, Hv, Dv;
+    int64_t steps;  // min(accepted, T): steps at or beyond it are never read
+    int rows_cta;
+    int64_t row_blocks;
+    int tc;
+};
+
+struct RepeatArgs {
+    const void *src;
+    void *dst;
+    int64_t seq, hg, h, row_bytes;
+    int elem_bytes;
+    bool vec16;     // rows are whole 16-byte vectors and both bases are 16-byte aligned
+};
+
+// Launch geometry for a tile layout with `rows_per_warp` rows per warp (host side).
+bool supported_dk(int64_t dk);
+int rows_per_warp(int dk);
+Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int sm_count);
+Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int sm_count);
+
+// One translation unit per element type keeps the (heavily unrolled) kernel
+// builds parallel.  Each returns cudaErrorInvalidValue for a Dk it lacks.
+cudaError_t launch_record_f32(int dk, const RecordArgs &a, const Geometry &geo, cudaStream_t s);
+cudaError_t launch_record_bf16(int dk, const RecordArgs &a, const Geometry &geo, cudaStream_t s);
+cudaError_t launch_record_f16(int dk, const RecordArgs &a, const Geometry &geo, cudaStream_t s);
+cudaError_t launch_replay(DType dt, int dk, const ReplayArgs &a, const Geometry &geo,
+                          cudaStream_t s);
+cudaError_t launch_repeat(const RepeatArgs &a, cudaStream_t s, int sm_count);
+
+}  // namespace gdn

@@ -1,0 +1,91 @@
+"""Helpers shared by the tests: device transfer and the comparison rule.
+
+Comparison rule (per element, float64):
+    |got - want| <= atol + rtol * |want|  (+ half a unit in the last place of
+    the stored type when the output is stored in bf16 / f16)
+with atol = rtol = 1e-4 for float32 problems and 1e-3 for bf16 / f16 inputs
+(the page's registered tolerance is 1e-3 for every dtype; float32 runs are
+held ten times tighter).  ``want`` is always the unrounded float64 oracle
+value; the half-ulp term admits a correctly rounded store of it.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import workloads
+
+TOL = {"f32": 1e-4, "bf16": 1e-3, "f16": 1e-3}
+SIG_BITS = {"f32": 24, "bf16": 8, "f16": 11}
+MIN_EXP = {"f32": -126, "bf16": -126, "f16": -14}
+
+
+def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Half the spacing of ``dtype`` values at magnitude |x| (0 for f32 outputs
+    compared against an f64 value is not used: f32 stores get the f32 ulp)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(np.maximum(ax, np.finfo(np.float64).tiny))
+    e = np.maximum(e, MIN_EXP[dtype] + 1)
+    return np.ldexp(1.0, e - SIG_BITS[dtype] - 1)
+
+
+def excess(got, want, in_dtype: str, stored: str | None = None) -> np.ndarray:
+    """Per-element amount by which |got - want| exceeds the bound (<= 0 passes)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    t = TOL[in_dtype]
+    bound = t + t * np.abs(want)
+    if stored is not None:
+        bound = bound + half_ulp(np.maximum(np.abs(want), np.abs(got)), stored)
+    return np.abs(got - want) - bound
+
+
+def assert_close(got, want, in_dtype: str, stored: str | None = None, what: str = ""):
+    ex = excess(got, want, in_dtype, stored)
+    if ex.size and not (ex <= 0).all():
+        bad = np.argwhere(~(ex <= 0))
+        i = tuple(bad[0])
+        raise AssertionError(
+            f"{what}: {len(bad)} of {ex.size} elements out of tolerance; first at {i}: "
+            f"got {np.asarray(got)[i]!r} want {np.asarray(want)[i]!r} (excess {ex[i]:.3e})")
+
+
+def torch_dtype(dtype: str):
+    import torch
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+
+
+def to_dev(arr: np.ndarray, dev):
+    """Storage array (see workloads) -> torch tensor on ``dev``, same bits."""
+    import torch
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16).to(dev)
+    if arr.dtype == np.uint32:
+        return torch.from_numpy(np.ascontiguousarray(arr).astype(np.int32)).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(arr)).to(dev)
+
+
+def to_host_f64(t) -> np.ndarray:
+    import torch
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def storage_of(t) -> np.ndarray:
+    """Torch tensor -> numpy array in workloads' storage form (bf16 as uint16 bits)."""
+    import torch
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 values through float32 to the storage type; storage array."""
+    return workloads.to_storage(np.asarray(x, dtype=np.float64).astype(np.float32), dtype)
+
+
+def device_inputs(case, dev):
+    """q, k, v, g, beta, state, mask of a workloads.Case on ``dev``."""
+    q, k, v, g, beta = (to_dev(getattr(case, n), dev) for n in ("q", "k", "v", "g", "beta"))
+    state = to_dev(case.state, dev)
+    mask = None if case.mask is None else to_dev(case.mask, dev)
+    return q, k, v, g, beta, state, mask

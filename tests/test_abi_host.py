@@ -1,0 +1,172 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+* libgdn.so builds for sm_103a, loads, and exports every function that
+  include/gdn.h declares;
+* every argument check of include/gdn.h returns its status before anything
+  is launched.  Each call below carries at least one invalid argument, so it
+  can never reach a kernel (the fake pointers are never dereferenced).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_recurrence_step_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA = 0, 1, 2, 3, 4
+F32, BF16, F16 = 0, 1, 2
+A = 0x10000  # fake, 16-byte aligned device addresses (never dereferenced)
+
+
+def P(i: int) -> int:
+    return A * (i + 1)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gdn.build()
+    return gdn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    names = re.findall(r"^[A-Za-z_][\w \t\*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("gdn_step_record", "gdn_state_replay", "gqa_repeat_tiled",
+                 "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libgdn.so does not export {name}"
+    assert lib.gdn_abi_version() == 1
+
+
+def test_library_is_sm103a():
+    # the build passes exactly one -gencode, for sm_103a
+    from linear_attention_recurrence_step_gb300 import _build
+    assert _build.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert os.path.exists(_build.LIB_PATH)
+
+
+def test_status_strings(lib):
+    for code, name in gdn.STATUS_NAMES.items():
+        assert lib.gdn_status_string(code).decode() == name
+
+
+def rec(lib, **kw):
+    args = dict(q=P(0), k=P(1), v=P(2), g=P(3), beta=P(4), state_in=P(5), mask=None,
+                y=P(6), state_out=P(7), delta_log=P(8), k_log=None, g_log=None,
+                B=2, T=3, Hk=2, Hv=4, Dk=64, Dv=32, dtype=BF16, stream=None)
+    args.update(kw)
+    return lib.gdn_step_record(*args.values())
+
+
+def rep(lib, **kw):
+    args = dict(delta_log=P(0), k_log=P(1), g_log=P(2), state_in=P(3), mask=None,
+                state_out=P(4), B=2, T=3, Hv=4, Dk=64, Dv=32, accepted=2, dtype=BF16,
+                stream=None)
+    args.update(kw)
+    return lib.gdn_state_replay(*args.values())
+
+
+def rpt(lib, **kw):
+    args = dict(src=P(0), dst=P(8), seq=4, hg=2, h=6, k=8, dtype=F32,
+                src_bytes=4 * 2 * 8 * 4, dst_bytes=4 * 6 * 8 * 4, stream=None)
+    args.update(kw)
+    return lib.gqa_repeat_tiled(*args.values())
+
+
+RECORD_CASES = {
+    "B=0": (dict(B=0), INVALID),
+    "T=0": (dict(T=0), INVALID),
+    "Hk=0": (dict(Hk=0), INVALID),
+    "Dv=-1": (dict(Dv=-1), INVALID),
+    "Hv%Hk": (dict(Hk=3), INVALID),
+    "null q": (dict(q=None), INVALID),
+    "null state_out": (dict(state_out=None), INVALID),
+    "null delta_log": (dict(delta_log=None), INVALID),
+    "Dk%32": (dict(Dk=48), UNSUPPORTED),
+    "Dk=96 not compiled": (dict(Dk=96), UNSUPPORTED),
+    "Dk=512 not compiled": (dict(Dk=512), UNSUPPORTED),
+    "dtype": (dict(dtype=9), UNSUPPORTED),
+    "overflow": (dict(B=1 << 40, T=1 << 20), INVALID),
+    "q misaligned": (dict(q=P(0) + 4), MISALIGNED),
+    "state_in misaligned": (dict(state_in=P(5) + 8), MISALIGNED),
+    "v odd address bf16": (dict(v=P(2) + 1), MISALIGNED),
+    "mask misaligned": (dict(mask=P(9) + 2), MISALIGNED),
+    "state overlap": (dict(state_out=P(5) + 16), INVALID),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RECORD_CASES))
+def test_record_rejects(lib, name):
+    kw, want = RECORD_CASES[name]
+    assert rec(lib, **kw) == want
+    assert lib.gdn_last_error().decode().startswith("gdn_step_record")
+
+
+REPLAY_CASES = {
+    "B=0": (dict(B=0), INVALID),
+    "Dv=0": (dict(Dv=0), INVALID),
+    "accepted<0": (dict(accepted=-1), INVALID),
+    "null k_log": (dict(k_log=None), INVALID),
+    "null g_log": (dict(g_log=None), INVALID),
+    "Dk=80": (dict(Dk=80), UNSUPPORTED),
+    "dtype": (dict(dtype=-1), UNSUPPORTED),
+    "k_log misaligned": (dict(k_log=P(1) + 2), MISALIGNED),
+    "state overlap": (dict(state_out=P(3) + 32), INVALID),
+    "overflow": (dict(B=1 << 50, Dv=1 << 20), INVALID),
+}
+
+
+@pytest.mark.parametrize("name", sorted(REPLAY_CASES))
+def test_replay_rejects(lib, name):
+    kw, want = REPLAY_CASES[name]
+    assert rep(lib, **kw) == want
+    assert lib.gdn_last_error().decode().startswith("gdn_state_replay")
+
+
+REPEAT_CASES = {
+    # the error rules of dispatch_repeat_tiled_f32 ("mlx-native repeat_tiled.rs")
+    "seq=0": (dict(seq=0), INVALID),
+    "hg=0": (dict(hg=0), INVALID),
+    "h=0": (dict(h=0), INVALID),
+    "k=0": (dict(k=0), INVALID),
+    "h%hg": (dict(h=5), INVALID),
+    "src too small": (dict(src_bytes=4 * 2 * 8 * 4 - 1), INVALID),
+    "dst too small": (dict(dst_bytes=4 * 6 * 8 * 4 - 4), INVALID),
+    "src overflow": (dict(seq=1 << 40, k=1 << 30), INVALID),
+    "null src": (dict(src=None), INVALID),
+    "overlap": (dict(dst=P(0) + 64), INVALID),
+    "dtype": (dict(dtype=5), UNSUPPORTED),
+    "misaligned f32": (dict(src=P(0) + 2), MISALIGNED),
+}
+
+
+@pytest.mark.parametrize("name", sorted(REPEAT_CASES))
+def test_repeat_rejects(lib, name):
+    kw, want = REPEAT_CASES[name]
+    assert rpt(lib, **kw) == want
+    msg = lib.gdn_last_error().decode()
+    assert msg.startswith("gqa_repeat_tiled")
+    if name == "src too small":
+        assert "need 256 bytes, have 255" in msg
+
+
+def test_python_binding_refuses_without_library(tmp_path):
+    with pytest.raises(gdn.GdnError):
+        gdn.load(str(tmp_path / "missing.so"))

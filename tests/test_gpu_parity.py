@@ -1,0 +1,293 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Every comparison uses the rule of gdn_testutil (1e-4 abs + rel for float32
+problems, 1e-3 for bf16 / f16 inputs, plus half an output ulp for values
+stored in bf16 / f16).  Inputs come from workloads (seeded, synthetic); no
+expected value is ever taken from the GPU.
+
+Coverage:
+* the five named workloads at full size, in the launch configuration the
+  benchmark times: record outputs, the tape, k_log / g_log, masked slots
+  left untouched, replay on a host-made tape, the record -> replay chain;
+* a seeded sweep of small shapes (all compiled Dk, ragged Dv, T across the
+  16-step staging chunks, every dtype, masks);
+* edge cases: g = 0 resets, the scaled-state fallback (products of g below
+  2^-32, g > 1), accepted = 0 / beyond T, all-masked, NaN in unused tape
+  slots, in-place state, bit-exact record -> replay for float32 tapes,
+  run-to-run determinism, the tiled repeat (bit-exact).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gdn_testutil import (assert_close, device_inputs, round_to, storage_of, to_dev,
+                          to_host_f64, torch_dtype)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import linear_attention_recurrence_step_gb300 as gdn  # noqa: E402
+
+SENTINEL = float("nan")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdn.load()
+    return torch.device("cuda:0")
+
+
+def _alloc_outputs(case, dev, capture=True):
+    dt = torch_dtype(case.dtype)
+    B, T, Hv, Dv, Dk = case.B, case.T, case.Hv, case.Dv, case.Dk
+    out = dict(y=torch.full((B, T, Hv, Dv), SENTINEL, dtype=dt, device=dev),
+               delta_log=torch.full((B, T, Hv, Dv), SENTINEL, dtype=dt, device=dev),
+               state_out=torch.full((B, Hv, Dv, Dk), SENTINEL, dtype=torch.float32, device=dev))
+    if capture:
+        out["k_log"] = torch.full((B, T, Hv, Dk), SENTINEL, dtype=dt, device=dev)
+        out["g_log"] = torch.full((B, T, Hv), SENTINEL, dtype=dt, device=dev)
+    return out
+
+
+def _oracle_inputs(case, q_override=None, k_override=None, hk=None):
+    q = case.f64("q") if q_override is None else q_override
+    k = case.f64("k") if k_override is None else k_override
+    return q, k, case.f64("v"), case.f64("g"), case.f64("beta"), case.f64("state"), case.mask
+
+
+def _active(case):
+    if case.mask is None:
+        return np.ones((case.B, case.T), dtype=bool)
+    return case.mask.astype(bool)
+
+
+def _check_record(case, got, ref, capture=True, k_expanded=None, g_in=None):
+    """Compare one GPU record against the oracle, including untouched slots."""
+    act = _active(case)
+    dt = case.dtype
+    stored = None if dt == "f32" else dt
+    y = to_host_f64(got["y"])
+    dl = to_host_f64(got["delta_log"])
+    assert_close(to_host_f64(got["state_out"]), ref["state_out"], dt, None, "state_out")
+    assert_close(y[act], ref["y"][act], dt, stored, "y")
+    assert_close(dl[act], ref["delta_log"][act], dt, stored, "delta_log")
+    assert np.isnan(y[~act]).all() and np.isnan(dl[~act]).all(), "masked y/delta_log were written"
+    if capture:
+        kl = to_host_f64(got["k_log"])
+        gl = to_host_f64(got["g_log"])
+        np.testing.assert_array_equal(kl[act], ref["k_log"][act])
+        np.testing.assert_array_equal(gl[act], ref["g_log"][act])
+        assert np.isnan(kl[~act]).all() and np.isnan(gl[~act]).all()
+
+
+def _run_record(case, dev, capture=True, q=None, k=None, Hk=None):
+    dq, dk_, v, g, beta, s0, mask = device_inputs(case, dev)
+    if q is not None:
+        dq, dk_ = q, k
+    out = _alloc_outputs(case, dev, capture)
+    gdn.gdn_step_record(dq, dk_, v, g, beta, s0, mask, **out)
+    torch.cuda.synchronize()
+    return out, s0, mask
+
+
+# ------------------------------------------------------------ named configs
+@pytest.mark.parametrize("name", workloads.CONFIG_ORDER)
+def test_named_workload(dev, name):
+    case = workloads.make_config(name)
+    dt = case.dtype
+    if workloads.uses_repeat(name):
+        # tiled GQA expansion of q / k to Hv heads on the GPU, then record with
+        # Hk' = Hv (so hk = hv): the mapping the expanded layout implies.
+        Hv = case.Hv
+        qd, kd = to_dev(case.q, dev), to_dev(case.k, dev)
+        qx = gdn.gqa_repeat_tiled(qd.reshape(case.B * case.T, case.Hk, case.Dk), Hv)
+        kx = gdn.gqa_repeat_tiled(kd.reshape(case.B * case.T, case.Hk, case.Dk), Hv)
+        qx = qx.reshape(case.B, case.T, Hv, case.Dk)
+        kx = kx.reshape(case.B, case.T, Hv, case.Dk)
+        q_ref = oracle.repeat_tiled(case.q.reshape(case.B * case.T, case.Hk, case.Dk), Hv)
+        k_ref = oracle.repeat_tiled(case.k.reshape(case.B * case.T, case.Hk, case.Dk), Hv)
+        np.testing.assert_array_equal(storage_of(qx).reshape(q_ref.shape), q_ref)
+        np.testing.assert_array_equal(storage_of(kx).reshape(k_ref.shape), k_ref)
+        q64 = workloads.widen(q_ref, dt).reshape(case.B, case.T, Hv, case.Dk)
+        k64 = workloads.widen(k_ref, dt).reshape(case.B, case.T, Hv, case.Dk)
+        case_x = workloads.Case(**{**case.__dict__, "Hk": Hv,
+                                   "q": q_ref.reshape(case.B, case.T, Hv, case.Dk),
+                                   "k": k_ref.reshape(case.B, case.T, Hv, case.Dk)})
+        got, s0, mask = _run_record(case_x, dev, q=qx, k=kx)
+        ref = oracle.record(q64, k64, *_oracle_inputs(case)[2:])
+        _check_record(case_x, got, ref)
+    else:
+        got, s0, mask = _run_record(case, dev)
+        ref = oracle.record(*_oracle_inputs(case))
+        _check_record(case, got, ref)
+
+    # replay on a tape made on the host (the oracle's delta in the tape dtype)
+    acc = case.accepted
+    tape = round_to(np.nan_to_num(ref["delta_log"]), dt)
+    kl = round_to(np.nan_to_num(ref["k_log"]), dt)
+    gl = round_to(np.nan_to_num(ref["g_log"]), dt)
+    st = gdn.gdn_state_replay(to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev), s0, mask,
+                              accepted=acc)
+    ref_st = oracle.replay(workloads.widen(tape, dt), workloads.widen(kl, dt),
+                           workloads.widen(gl, dt), case.f64("state"), case.mask, accepted=acc)
+    assert_close(to_host_f64(st), ref_st, dt, None, "replay(host tape)")
+
+    # the chain the method runs: GPU record's own tape -> GPU replay, against
+    # the oracle's chain (record, tape rounded to dtype, replay)
+    st2 = gdn.gdn_state_replay(got["delta_log"], got["k_log"], got["g_log"], s0, mask,
+                               accepted=acc)
+    assert_close(to_host_f64(st2), ref_st, dt, None, "record->replay chain")
+
+
+# ------------------------------------------------------------ seeded sweep
+def _sweep_cases():
+    rng = np.random.default_rng(2024)
+    cases = []
+    dks = [32, 64, 128, 192, 256]
+    dvs = [1, 5, 32, 48, 100, 128, 200]
+    for i in range(24):
+        dt = ["f32", "bf16", "f16"][i % 3]
+        Dk = dks[i % len(dks)]
+        Dv = dvs[(i * 3) % len(dvs)]
+        Hk = int(rng.choice([1, 2, 4]))
+        Hv = Hk * int(rng.choice([1, 2, 3]))
+        B = int(rng.integers(1, 4))
+        T = int(rng.choice([1, 2, 7, 16, 17, 37]))
+        mask = ["none", "bernoulli:0.6", "prefix", "all_on"][i % 4]
+        cases.append(dict(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, dtype=dt, seed=500 + i,
+                          mask=mask, accepted="uniform"))
+    return cases
+
+
+@pytest.mark.parametrize("spec", _sweep_cases(),
+                         ids=lambda s: f"{s['dtype']}-Dk{s['Dk']}-Dv{s['Dv']}-B{s['B']}T{s['T']}"
+                                       f"Hk{s['Hk']}Hv{s['Hv']}-{s['mask']}")
+def test_sweep(dev, spec):
+    case = workloads.make_case(**spec)
+    got, s0, mask = _run_record(case, dev)
+    ref = oracle.record(*_oracle_inputs(case))
+    _check_record(case, got, ref)
+    tape = round_to(np.nan_to_num(ref["delta_log"]), case.dtype)
+    kl = round_to(np.nan_to_num(ref["k_log"]), case.dtype)
+    gl = round_to(np.nan_to_num(ref["g_log"]), case.dtype)
+    st = gdn.gdn_state_replay(to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev), s0, mask,
+                              accepted=case.accepted)
+    ref_st = oracle.replay(workloads.widen(tape, case.dtype), workloads.widen(kl, case.dtype),
+                           workloads.widen(gl, case.dtype), case.f64("state"), case.mask,
+                           accepted=case.accepted)
+    assert_close(to_host_f64(st), ref_st, case.dtype, None, "replay")
+
+
+# ------------------------------------------------------------ edge cases
+def test_decay_edges(dev):
+    """g = 0 (reset), long products of g below the 2^-32 scale limit, g > 1."""
+    for seed, T, g_range in [(1, 6, (0.0, 0.0)), (2, 80, (0.3, 0.5)), (3, 200, (1.05, 1.25)),
+                             (4, 300, (0.6, 1.0))]:
+        case = workloads.make_case(B=2, T=T, Hk=1, Hv=2, Dk=64, Dv=40, dtype="f32", seed=seed,
+                                   g_range=g_range, mask="bernoulli:0.9")
+        got, s0, mask = _run_record(case, dev)
+        ref = oracle.record(*_oracle_inputs(case))
+        _check_record(case, got, ref)
+        st = gdn.gdn_state_replay(got["delta_log"], got["k_log"], got["g_log"], s0, mask,
+                                  accepted=T)
+        assert torch.equal(st, got["state_out"]), f"bit-exact replay, seed {seed}"
+
+
+def test_f32_record_replay_bit_exact(dev):
+    case = workloads.make_case(B=3, T=21, Hk=2, Hv=4, Dk=128, Dv=72, dtype="f32", seed=9,
+                               mask="bernoulli:0.7")
+    got, s0, mask = _run_record(case, dev)
+    for acc in (case.T, case.T + 5):
+        st = gdn.gdn_state_replay(got["delta_log"], got["k_log"], got["g_log"], s0, mask,
+                                  accepted=acc)
+        assert torch.equal(st, got["state_out"])
+    # accepted = a equals a record over the first a steps, bit for bit
+    for a in (1, 8, 16, 17):
+        sub = workloads.Case(**{**case.__dict__, "T": a, "q": case.q[:, :a], "k": case.k[:, :a],
+                                "v": case.v[:, :a], "g": case.g[:, :a], "beta": case.beta[:, :a],
+                                "mask": case.mask[:, :a]})
+        got_a, _, _ = _run_record(sub, dev)
+        st = gdn.gdn_state_replay(got["delta_log"], got["k_log"], got["g_log"], s0, mask,
+                                  accepted=a)
+        assert torch.equal(st, got_a["state_out"]), f"accepted={a}"
+
+
+def test_accepted_zero_and_all_masked(dev):
+    case = workloads.make_case(B=2, T=5, Hk=2, Hv=4, Dk=128, Dv=128, dtype="bf16", seed=11,
+                               mask="all_off")
+    got, s0, mask = _run_record(case, dev)
+    assert torch.equal(got["state_out"], s0)
+    assert torch.isnan(got["y"].float()).all() and torch.isnan(got["delta_log"].float()).all()
+    st = gdn.gdn_state_replay(got["delta_log"], got["k_log"], got["g_log"], s0, None, accepted=0)
+    assert torch.equal(st, s0)
+    s1 = s0.clone()
+    gdn.gdn_state_replay(got["delta_log"], got["k_log"], got["g_log"], s1, None, accepted=0,
+                         state_out=s1)
+    assert torch.equal(s1, s0)
+
+
+def test_nan_in_unused_tape_slots(dev):
+    case = workloads.make_case(B=3, T=9, Hk=2, Hv=4, Dk=64, Dv=64, dtype="bf16", seed=12,
+                               mask="bernoulli:0.5", accepted=6)
+    got, s0, mask = _run_record(case, dev)
+    clean = gdn.gdn_state_replay(got["delta_log"], got["k_log"], got["g_log"], s0, mask,
+                                 accepted=6)
+    dl, kl, gl = got["delta_log"].clone(), got["k_log"].clone(), got["g_log"].clone()
+    off = ~torch.from_numpy(case.mask.astype(bool)).to(dev)
+    off[:, 6:] = True                       # unaccepted steps too
+    dl[off] = float("nan")
+    kl[off] = float("nan")
+    gl[off] = float("nan")
+    dirty = gdn.gdn_state_replay(dl, kl, gl, s0, mask, accepted=6)
+    assert torch.equal(dirty, clean)
+
+
+def test_in_place_state(dev):
+    case = workloads.make_config("spec_verify_b16_t8_bf16", batch=4)
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    ref = gdn.gdn_step_record(q, k, v, g, beta, s0, mask, capture_tape=True)
+    s_inplace = s0.clone()
+    out = gdn.gdn_step_record(q, k, v, g, beta, s_inplace, mask, state_out=s_inplace,
+                              capture_tape=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out.state_out, ref.state_out)
+    snap = s0.clone()
+    gdn.gdn_state_replay(ref.delta_log, ref.k_log, ref.g_log, snap, mask,
+                         accepted=case.accepted, state_out=snap)
+    st = gdn.gdn_state_replay(ref.delta_log, ref.k_log, ref.g_log, s0, mask,
+                              accepted=case.accepted)
+    assert torch.equal(snap, st)
+
+
+def test_determinism(dev):
+    case = workloads.make_config("rollback_b128_t16_bf16", batch=8)
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    a = gdn.gdn_step_record(q, k, v, g, beta, s0, mask, capture_tape=True)
+    b = gdn.gdn_step_record(q, k, v, g, beta, s0, mask, capture_tape=True)
+    torch.cuda.synchronize()
+    on = torch.from_numpy(case.mask.astype(bool)).to(dev)
+    assert torch.equal(a.state_out, b.state_out)
+    assert torch.equal(a.y[on], b.y[on]) and torch.equal(a.delta_log[on], b.delta_log[on])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_repeat_bit_exact(dev, dtype):
+    rng = np.random.default_rng(77)
+    for seq, hg, h, kd in [(4096, 16, 32, 128), (3, 1, 5, 7), (17, 3, 12, 9), (5, 4, 4, 64),
+                           (2, 2, 8, 1)]:
+        src = workloads.to_storage(rng.standard_normal((seq, hg, kd)).astype(np.float32), dtype)
+        want = oracle.repeat_tiled(src, h)
+        got = gdn.gqa_repeat_tiled(to_dev(src, dev), h)
+        np.testing.assert_array_equal(storage_of(got), want)
+    # an offset view (not 16-byte aligned) takes the element path
+    src = workloads.to_storage(rng.standard_normal((6 * 2 * 8 + 1,)).astype(np.float32), dtype)
+    base = to_dev(src, dev)
+    view = base[1:].view(6, 2, 8)
+    got = gdn.gqa_repeat_tiled(view, 6)
+    want = oracle.repeat_tiled(src[1:].reshape(6, 2, 8), 6)
+    np.testing.assert_array_equal(storage_of(got), want)
