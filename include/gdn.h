@@ -92,8 +92,9 @@ typedef enum gdn_dtype {
  *              same pointer as state_in (in place); any other overlap with
  *              state_in is GDN_ERR_INVALID_ARGUMENT.
  *   delta_log  [B,T,Hv,Dv]  dtype (output, the innovation tape)
- *   k_log      [B,T,Hv,Dk]  dtype or NULL (output): k expanded to value heads,
- *              k_log[b,t,hv,:] = k[b,t,hv/G,:], written where delta_log is
+ *   k_log      [B,T,Hv,Dk]  dtype or NULL, 16-byte aligned (output): k
+ *              expanded to value heads, k_log[b,t,hv,:] = k[b,t,hv/G,:],
+ *              written where delta_log is
  *   g_log      [B,T,Hv]     dtype or NULL (output): copy of g, written where
  *              delta_log is
  *   Dk         32, 64, 128, 192 or 256 (else GDN_ERR_UNSUPPORTED); Dv any > 0

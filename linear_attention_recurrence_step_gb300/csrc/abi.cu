@@ -83,19 +83,30 @@ bool supported_dk(int64_t dk) {
 
 int rows_per_warp(int dk) {
     switch (dk) {
-    case 32: return TileLayout<32>::RW;
-    case 64: return TileLayout<64>::RW;
-    case 128: return TileLayout<128>::RW;
-    case 192: return TileLayout<192>::RW;
-    case 256: return TileLayout<256>::RW;
+    case 32: return DefaultLayout<32>::type::RW;
+    case 64: return DefaultLayout<64>::type::RW;
+    case 128: return DefaultLayout<128>::type::RW;
+    case 192: return DefaultLayout<192>::type::RW;
+    case 256: return DefaultLayout<256>::type::RW;
     }
     return 0;
 }
 
+static int max_warps(int dk) {
+    switch (dk) {
+    case 32: return DefaultLayout<32>::type::MAX_WARPS;
+    case 64: return DefaultLayout<64>::type::MAX_WARPS;
+    case 128: return DefaultLayout<128>::type::MAX_WARPS;
+    case 192: return DefaultLayout<192>::type::MAX_WARPS;
+    case 256: return DefaultLayout<256>::type::MAX_WARPS;
+    }
+    return 1;
+}
+
 // Warps per CTA: a whole tile's rows when the grid still covers every SM
 // twice, fewer (rows of a tile split over several CTAs) when tiles are few.
-static int pick_warps(int rw, int64_t tiles, int64_t Dv, int sm_count) {
-    int nw = (int)std::min<int64_t>(TileLayout<128>::MAX_WARPS, ceil_div(Dv, rw));
+static int pick_warps(int dk, int rw, int64_t tiles, int64_t Dv, int sm_count) {
+    int nw = (int)std::min<int64_t>(max_warps(dk), ceil_div(Dv, rw));
     const int64_t want = 2 * (int64_t)(sm_count > 0 ? sm_count : 1);
     while (nw > 1 && tiles * ceil_div(Dv, (int64_t)nw * rw) < want) nw = (nw + 1) / 2;
     return nw;
@@ -103,27 +114,27 @@ static int pick_warps(int rw, int64_t tiles, int64_t Dv, int sm_count) {
 
 static constexpr int kChunk = 16;  // timesteps staged in shared memory at a time
 
-Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int sm_count) {
+Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int esize, int sm_count) {
     const int rw = rows_per_warp(dk);
-    const int nw = pick_warps(rw, tiles, Dv, sm_count);
+    const int nw = pick_warps(dk, rw, tiles, Dv, sm_count);
     Geometry g;
     g.threads = 32 * nw;
     g.rows_cta = nw * rw;
     g.row_blocks = ceil_div(Dv, g.rows_cta);
     g.tc = (int)std::min<int64_t>(T, kChunk);
-    g.smem = record_smem_bytes(dk, g.tc, g.rows_cta);
+    g.smem = record_smem_bytes(dk, g.tc, g.rows_cta, esize);
     return g;
 }
 
-Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int sm_count) {
+Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int esize, int sm_count) {
     const int rw = rows_per_warp(dk);
-    const int nw = pick_warps(rw, tiles, Dv, sm_count);
+    const int nw = pick_warps(dk, rw, tiles, Dv, sm_count);
     Geometry g;
     g.threads = 32 * nw;
     g.rows_cta = nw * rw;
     g.row_blocks = ceil_div(Dv, g.rows_cta);
     g.tc = (int)std::max<int64_t>(1, std::min<int64_t>(steps, kChunk));
-    g.smem = replay_smem_bytes(dk, g.tc, g.rows_cta);
+    g.smem = replay_smem_bytes(dk, g.tc, g.rows_cta, esize);
     return g;
 }
 
@@ -169,14 +180,14 @@ gdn_status gdn_step_record(const void *q, const void *k, const void *v, const vo
     const int64_t qk_b = nbytes({B, T, Hk, Dk}, eb), v_b = nbytes({B, T, Hv, Dv}, eb);
     const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), kl_b = nbytes({B, T, Hv, Dk}, eb);
     const int64_t gb_b = nbytes({B, T, Hv}, eb), m_b = nbytes({B, T}, 4);
-    int64_t blocks_bound = 0;
-    if (qk_b < 0 || v_b < 0 || s_b < 0 || kl_b < 0 || gb_b < 0 || m_b < 0 ||
-        !mul_ok(B * Hv, Dv, &blocks_bound))
+    if (qk_b < 0 || v_b < 0 || s_b < 0 || kl_b < 0 || gb_b < 0 || m_b < 0)
         return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: tensor sizes overflow int64");
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(state_in, 16) || !aligned(state_out, 16))
-        return fail(GDN_ERR_MISALIGNED, "gdn_step_record: q, k, state_in, state_out must be 16-byte aligned");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(state_in, 16) || !aligned(state_out, 16) ||
+        !aligned(k_log, 16))
+        return fail(GDN_ERR_MISALIGNED,
+                    "gdn_step_record: q, k, state_in, state_out, k_log must be 16-byte aligned");
     if (!aligned(v, eb) || !aligned(g, eb) || !aligned(beta, eb) || !aligned(y, eb) ||
-        !aligned(delta_log, eb) || !aligned(k_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4))
+        !aligned(delta_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4))
         return fail(GDN_ERR_MISALIGNED, "gdn_step_record: a tensor is not aligned to its element size");
     if (state_in != state_out && overlap(state_in, s_b, state_out, s_b))
         return fail(GDN_ERR_INVALID_ARGUMENT,
@@ -185,11 +196,12 @@ gdn_status gdn_step_record(const void *q, const void *k, const void *v, const vo
     cudaError_t e;
     const int sms = current_sm_count(&e);
     if (e != cudaSuccess) return cuda_fail("gdn_step_record: device query", e);
-    const gdn::Geometry geo = gdn::record_geometry((int)Dk, B * Hv, Dv, T, sms);
+    const gdn::Geometry geo = gdn::record_geometry((int)Dk, B * Hv, Dv, T, eb, sms);
     if ((B * Hv) > (int64_t)INT32_MAX / geo.row_blocks)
         return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: grid too large (B*Hv*row_blocks > 2^31-1)");
     gdn::RecordArgs a{q, k, v, g, beta, state_in, mask, y, state_out, delta_log, k_log, g_log,
-                      B, T, Hk, Hv, Dv, geo.rows_cta, geo.row_blocks, geo.tc};
+                      B, T, Hk, Hv, Dv, geo.rows_cta, geo.row_blocks, geo.tc,
+                      aligned(v, 16) && (Dv * eb) % 16 == 0};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (dtype) {
     case GDN_DTYPE_F32: e = gdn::launch_record_f32((int)Dk, a, geo, s); break;
@@ -237,11 +249,12 @@ gdn_status gdn_state_replay(const void *delta_log, const void *k_log, const void
     cudaError_t e;
     const int sms = current_sm_count(&e);
     if (e != cudaSuccess) return cuda_fail("gdn_state_replay: device query", e);
-    const gdn::Geometry geo = gdn::replay_geometry((int)Dk, B * Hv, Dv, steps, sms);
+    const gdn::Geometry geo = gdn::replay_geometry((int)Dk, B * Hv, Dv, steps, eb, sms);
     if ((B * Hv) > (int64_t)INT32_MAX / geo.row_blocks)
         return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay: grid too large");
     gdn::ReplayArgs a{delta_log, k_log, g_log, state_in, mask, state_out, B, T, Hv, Dv, steps,
-                      geo.rows_cta, geo.row_blocks, geo.tc};
+                      geo.rows_cta, geo.row_blocks, geo.tc,
+                      aligned(delta_log, 16) && (Dv * eb) % 16 == 0};
     e = gdn::launch_replay(static_cast<gdn::DType>(dtype), (int)Dk, a, geo,
                            reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail("gdn_state_replay: launch", e);

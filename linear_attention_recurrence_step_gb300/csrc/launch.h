@@ -31,6 +31,7 @@ struct RecordArgs {
     int rows_cta;
     int64_t row_blocks;
     int tc;
+    bool vec_v;     // v rows can be copied in 16-byte pieces (aligned base, Dv*size % 16 == 0)
 };
 
 struct ReplayArgs {
@@ -43,6 +44,7 @@ struct ReplayArgs {
     int rows_cta;
     int64_t row_blocks;
     int tc;
+    bool vec_d;     // delta_log rows can be copied in 16-byte pieces
 };
 
 struct RepeatArgs {
@@ -56,8 +58,9 @@ struct RepeatArgs {
 // Launch geometry for a tile layout with `rows_per_warp` rows per warp (host side).
 bool supported_dk(int64_t dk);
 int rows_per_warp(int dk);
-Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int sm_count);
-Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int sm_count);
+Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int esize, int sm_count);
+Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int esize,
+                         int sm_count);
 
 // One translation unit per element type keeps the (heavily unrolled) kernel
 // builds parallel.  Each returns cudaErrorInvalidValue for a Dk it lacks.

@@ -3,13 +3,18 @@
 
 namespace gdn {
 
+template <int DK>
+static cudaError_t run(const RecordArgs &a, const Geometry &geo, cudaStream_t s) {
+    return launch_record_layout<__half, typename DefaultLayout<DK>::type>(a, geo, s);
+}
+
 cudaError_t launch_record_f16(int dk, const RecordArgs &a, const Geometry &geo, cudaStream_t s) {
     switch (dk) {
-    case 32: return launch_record_t<__half, 32>(a, geo, s);
-    case 64: return launch_record_t<__half, 64>(a, geo, s);
-    case 128: return launch_record_t<__half, 128>(a, geo, s);
-    case 192: return launch_record_t<__half, 192>(a, geo, s);
-    case 256: return launch_record_t<__half, 256>(a, geo, s);
+    case 32: return run<32>(a, geo, s);
+    case 64: return run<64>(a, geo, s);
+    case 128: return run<128>(a, geo, s);
+    case 192: return run<192>(a, geo, s);
+    case 256: return run<256>(a, geo, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -3,14 +3,19 @@
 
 namespace gdn {
 
+template <typename TIn, int DK>
+static cudaError_t run(const ReplayArgs &a, const Geometry &geo, cudaStream_t s) {
+    return launch_replay_layout<TIn, typename DefaultLayout<DK>::type>(a, geo, s);
+}
+
 template <typename TIn>
 static cudaError_t replay_dk(int dk, const ReplayArgs &a, const Geometry &geo, cudaStream_t s) {
     switch (dk) {
-    case 32: return launch_replay_t<TIn, 32>(a, geo, s);
-    case 64: return launch_replay_t<TIn, 64>(a, geo, s);
-    case 128: return launch_replay_t<TIn, 128>(a, geo, s);
-    case 192: return launch_replay_t<TIn, 192>(a, geo, s);
-    case 256: return launch_replay_t<TIn, 256>(a, geo, s);
+    case 32: return run<TIn, 32>(a, geo, s);
+    case 64: return run<TIn, 64>(a, geo, s);
+    case 128: return run<TIn, 128>(a, geo, s);
+    case 192: return run<TIn, 192>(a, geo, s);
+    case 256: return run<TIn, 256>(a, geo, s);
     default: return cudaErrorInvalidValue;
     }
 }

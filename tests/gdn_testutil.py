@@ -28,25 +28,51 @@ def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
     return np.ldexp(1.0, e - SIG_BITS[dtype] - 1)
 
 
-def excess(got, want, in_dtype: str, stored: str | None = None) -> np.ndarray:
-    """Per-element amount by which |got - want| exceeds the bound (<= 0 passes)."""
+def excess(got, want, in_dtype: str, stored: str | None = None, extra=None) -> np.ndarray:
+    """Per-element amount by which |got - want| exceeds the bound (<= 0 passes).
+    ``extra`` adds a derived per-element bound (e.g. tape_rounding_bound)."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     t = TOL[in_dtype]
     bound = t + t * np.abs(want)
+    if extra is not None:
+        bound = bound + extra
     if stored is not None:
         bound = bound + half_ulp(np.maximum(np.abs(want), np.abs(got)), stored)
     return np.abs(got - want) - bound
 
 
-def assert_close(got, want, in_dtype: str, stored: str | None = None, what: str = ""):
-    ex = excess(got, want, in_dtype, stored)
+def assert_close(got, want, in_dtype: str, stored: str | None = None, what: str = "",
+                 extra=None):
+    ex = excess(got, want, in_dtype, stored, extra)
     if ex.size and not (ex <= 0).all():
         bad = np.argwhere(~(ex <= 0))
         i = tuple(bad[0])
         raise AssertionError(
             f"{what}: {len(bad)} of {ex.size} elements out of tolerance; first at {i}: "
             f"got {np.asarray(got)[i]!r} want {np.asarray(want)[i]!r} (excess {ex[i]:.3e})")
+
+
+def tape_rounding_bound(k_log, g_log, delta, mask, accepted: int, dtype: str) -> np.ndarray:
+    """Per-element bound on how far two replays can drift apart when their
+    delta tapes were rounded to ``dtype`` independently (the GPU rounds its
+    f32 delta, the oracle path rounds its f64 delta): each tape entry may land
+    on the neighbouring representable value, one ulp away, and replay carries
+    that error as  s <- g s + k (delta + e).  So
+        bound[b,hv,dv,i] = sum_t |k[b,t,hv,i]| ulp(delta[b,t,hv,dv]) prod_{t'>t} |g[b,t',hv]|
+    over the replayed (accepted, unmasked) steps.  Arrays are float64 oracle
+    values: k_log [B,T,Hv,Dk], g_log [B,T,Hv], delta [B,T,Hv,Dv]."""
+    B, T, Hv, Dv = delta.shape
+    Dk = k_log.shape[3]
+    act = np.ones((B, T), bool) if mask is None else mask.astype(bool)
+    bound = np.zeros((B, Hv, Dv, Dk))
+    for t in range(min(accepted, T)):
+        on = act[:, t][:, None, None, None]
+        ulp = 2.0 * half_ulp(np.nan_to_num(delta[:, t]), dtype)          # [B,Hv,Dv]
+        step = np.abs(np.nan_to_num(g_log[:, t]))[:, :, None, None] * bound + \
+            ulp[..., None] * np.abs(np.nan_to_num(k_log[:, t]))[:, :, None, :]
+        bound = np.where(on, step, bound)
+    return bound
 
 
 def torch_dtype(dtype: str):

@@ -108,6 +108,7 @@ RECORD_CASES = {
     "state_in misaligned": (dict(state_in=P(5) + 8), MISALIGNED),
     "v odd address bf16": (dict(v=P(2) + 1), MISALIGNED),
     "mask misaligned": (dict(mask=P(9) + 2), MISALIGNED),
+    "k_log misaligned": (dict(k_log=P(10) + 8), MISALIGNED),
     "state overlap": (dict(state_out=P(5) + 16), INVALID),
 }
 
