@@ -11,6 +11,7 @@
 #include "gdn.h"
 #include "launch.h"
 #include "record.cuh"
+#include "record_mma.cuh"
 #include "replay.cuh"
 
 namespace {
@@ -112,9 +113,23 @@ static int pick_warps(int dk, int rw, int64_t tiles, int64_t Dv, int sm_count) {
     return nw;
 }
 
-static constexpr int kChunk = 16;  // timesteps staged in shared memory at a time
+static constexpr int kChunk = 16;        // timesteps staged in shared memory at a time
+static constexpr int kMmaMinSteps = 12;  // shortest call routed to the tensor-core kernel
 
-Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int esize, int sm_count) {
+Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int esize, bool bf16,
+                         int sm_count) {
+    // the tensor-core chunk kernel pays for its 16-step chunk machinery only
+    // when calls carry enough steps; short calls take the FP32 kernel
+    if (bf16 && record_mma_supported(dk) && T >= kMmaMinSteps) {
+        Geometry g;
+        g.threads = 32 * kMmaWarps;
+        g.rows_cta = kMmaRows;
+        g.row_blocks = ceil_div(Dv, g.rows_cta);
+        g.tc = kMmaChunk;
+        g.smem = record_mma_smem_bytes(dk);
+        g.mma = true;
+        return g;
+    }
     const int rw = rows_per_warp(dk);
     const int nw = pick_warps(dk, rw, tiles, Dv, sm_count);
     Geometry g;
@@ -123,6 +138,7 @@ Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int esize
     g.row_blocks = ceil_div(Dv, g.rows_cta);
     g.tc = (int)std::min<int64_t>(T, kChunk);
     g.smem = record_smem_bytes(dk, g.tc, g.rows_cta, esize);
+    g.mma = false;
     return g;
 }
 
@@ -135,6 +151,7 @@ Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int e
     g.row_blocks = ceil_div(Dv, g.rows_cta);
     g.tc = (int)std::max<int64_t>(1, std::min<int64_t>(steps, kChunk));
     g.smem = replay_smem_bytes(dk, g.tc, g.rows_cta, esize);
+    g.mma = false;
     return g;
 }
 
@@ -196,7 +213,8 @@ gdn_status gdn_step_record(const void *q, const void *k, const void *v, const vo
     cudaError_t e;
     const int sms = current_sm_count(&e);
     if (e != cudaSuccess) return cuda_fail("gdn_step_record: device query", e);
-    const gdn::Geometry geo = gdn::record_geometry((int)Dk, B * Hv, Dv, T, eb, sms);
+    const gdn::Geometry geo =
+        gdn::record_geometry((int)Dk, B * Hv, Dv, T, eb, dtype == GDN_DTYPE_BF16, sms);
     if ((B * Hv) > (int64_t)INT32_MAX / geo.row_blocks)
         return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: grid too large (B*Hv*row_blocks > 2^31-1)");
     gdn::RecordArgs a{q, k, v, g, beta, state_in, mask, y, state_out, delta_log, k_log, g_log,

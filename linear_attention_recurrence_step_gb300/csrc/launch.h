@@ -18,6 +18,7 @@ struct Geometry {
     int64_t row_blocks; // ceil(Dv / rows_cta)
     int tc;             // staged chunk length in timesteps
     size_t smem;        // dynamic shared memory bytes
+    bool mma;           // record: the tensor-core chunk kernel (bf16 inputs)
 };
 
 struct RecordArgs {
@@ -58,7 +59,8 @@ struct RepeatArgs {
 // Launch geometry for a tile layout with `rows_per_warp` rows per warp (host side).
 bool supported_dk(int64_t dk);
 int rows_per_warp(int dk);
-Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int esize, int sm_count);
+Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int esize, bool bf16,
+                         int sm_count);
 Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int esize,
                          int sm_count);
 

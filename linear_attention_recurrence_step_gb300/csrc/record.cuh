@@ -64,8 +64,6 @@ record_kernel(const RecordArgs a) {
     const int my_lr = lr0 + my_m;
     const bool my_store = (REDV == 2 || (j & 1) == 0) && my_lr < vlim;
     const int src0 = lane & ~(L - 1);                    // first lane of the row group
-    const int perm = row_perm<Lay>(j);                   // slot m holds row lr0 + (m ^ perm)
-    const bool swapkq = REDV == 1 && (j & 1);            // odd lanes sum q first (see transpose_reduce)
 
     // ---- carve shared memory (ring slots addressed arithmetically: no
     // dynamically indexed pointer arrays, which would live in local memory)
@@ -132,7 +130,7 @@ record_kernel(const RecordArgs a) {
     // The state slice stays in registers for the whole launch.
     Slice<Lay> s;
     unsigned next_bits = issue(0);
-    load_rows<Lay>(s, a.state_in, n, a.Dv, row0 + lr0, j, perm);
+    load_rows<Lay>(s, a.state_in, n, a.Dv, row0 + lr0, j);
     float G_sched = 1.f;  // the scale schedule's running G (kept by the last warp)
 
     const int64_t nchunks = (a.T + TC - 1) / TC;
@@ -202,11 +200,11 @@ record_kernel(const RecordArgs a) {
         for (int tt = 0; tt < tcnt; ++tt) {
             if (!((bits >> tt) & 1u)) continue;  // uniform across the CTA
             const StepScalars S = sc[tt];
-            float4 kk[NCH], qq[NCH];  // the rows summed into pa / pb (k / q, swapped on odd lanes)
-            lane_chunks<Lay>(kk, (swapkq ? cQ : cK) + tt * DK, j);
-            lane_chunks<Lay>(qq, (swapkq ? cK : cQ) + tt * DK, j);
+            float4 kk[NCH], qq[NCH];
+            lane_chunks<Lay>(kk, cK + tt * DK, j);
+            lane_chunks<Lay>(qq, cQ + tt * DK, j);
 
-            // partial dots of every row slot over this lane's chunks
+            // a = s^.k and b = s^.q partials over this lane's chunks
             float2 pa[RT], pb[RT];
 #pragma unroll
             for (int m = 0; m < RT; ++m) pa[m] = pb[m] = make_float2(0.f, 0.f);
@@ -229,15 +227,15 @@ record_kernel(const RecordArgs a) {
                 red[2 * m] = pa[m].x + pa[m].y;
                 red[2 * m + 1] = pb[m].x + pb[m].y;
             }
-            transpose_reduce<Lay>(red);
+            transpose_reduce<Lay>(red, j);
             float A, Bq;  // s^.k and s^.q of this lane's row
             if (REDV == 2) {
                 A = red[0];
                 Bq = red[1];
             } else {
                 const float other = __shfl_xor_sync(0xffffffffu, red[0], 1);
-                A = swapkq ? other : red[0];
-                Bq = swapkq ? red[0] : other;
+                A = (j & 1) ? other : red[0];
+                Bq = (j & 1) ? red[0] : other;
             }
 
             // this lane's row: delta, y, the tape, and delta / G'
@@ -253,21 +251,13 @@ record_kernel(const RecordArgs a) {
             float d[RT];
 #pragma unroll
             for (int m = 0; m < RT; ++m)
-                d[m] = __shfl_sync(0xffffffffu, dmine,
-                                   src0 + (REDV == 2 ? (m ^ perm) : 2 * (m ^ perm)));
+                d[m] = __shfl_sync(0xffffffffu, dmine, src0 + (REDV == 2 ? m : 2 * m));
             if ((direct >> tt) & 1u) rescale_rows<Lay>(s, S.Gp);
-            if (REDV == 2) {
-                rank1_update<Lay>(s, kk, d);
-            } else {
-                float4 ku[NCH];
-#pragma unroll
-                for (int cc = 0; cc < NCH; ++cc) ku[cc] = swapkq ? qq[cc] : kk[cc];
-                rank1_update<Lay>(s, ku, d);
-            }
+            rank1_update<Lay>(s, kk, d);
         }
     }
     const float G = nchunks > 0 ? *s_gfinal : 1.f;
-    store_rows<Lay>(s, G, a.state_out, n, a.Dv, row0 + lr0, j, perm);
+    store_rows<Lay>(s, G, a.state_out, n, a.Dv, row0 + lr0, j);
 }
 
 template <typename TIn, class Lay>

@@ -1,10 +1,14 @@
 // record_bf16.cu -- record kernels with bf16 inputs / outputs (state f32).
 #include "record.cuh"
+#include "record_mma.cuh"
 
 namespace gdn {
 
 template <int DK>
 static cudaError_t run(const RecordArgs &a, const Geometry &geo, cudaStream_t s) {
+    if constexpr (record_mma_supported(DK)) {
+        if (geo.mma) return launch_record_mma<DK>(a, geo, s);
+    }
     return launch_record_layout<__nv_bfloat16, typename DefaultLayout<DK>::type>(a, geo, s);
 }
 

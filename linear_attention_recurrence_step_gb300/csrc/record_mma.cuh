@@ -1,0 +1,526 @@
+// record_mma.cuh -- the record kernel for bf16 inputs on the tensor cores
+// (warp-level mma.sync, bf16 x bf16 -> f32), 16 timesteps at a time.
+//
+// Over a chunk of C = 16 steps the recurrence of "metaltile-std
+// gated_delta_replay.rs" (kernel gated_delta_step_record) regroups into dense
+// contractions.  With the scaled state s = G s^ of record.cuh and
+// d_t = delta_t / G'_t:
+//     s^_t = s^_0 + sum_{u <= t} k_u d_u
+//     a_t  = s^_{t-1} . k_t = (S^_0 K^T)[t] + sum_{u < t} d_u (k_u . k_t)
+//     b_t  = s^_{t-1} . q_t = (S^_0 Q^T)[t] + sum_{u < t} d_u (k_u . q_t)
+//     kv = G'_t a_t,  delta_t = (v_t - kv) beta_t,  y_t = G'_t b_t + delta_t (k_t . q_t)
+// so a warp owning 16 state rows computes
+//   MMA1  P = S^_0 [K; Q]^T      (16 rows x 32 step-dots, K = Dk)
+//   a triangular solve per row over the chunk, using the chunk's Gram
+//         matrices KK[u][t] = k_u . k_t and KQ[u][t] = k_u . q_t
+//   MMA2  S^ += D K              (16 rows x Dk, K = the 16 steps)
+// and the FP32 pipes do O(C) work per row instead of O(C Dk).
+//
+// Precision: k and q are bf16 inputs, exact as MMA operands.  The f32 state
+// and the f32 d values are split into two bf16 terms (hi + lo, 16
+// significant bits) for the products; every product is exact in the f32
+// accumulator, and the state itself stays f32 in the accumulator fragments.
+//
+// Register layout (m16n8 accumulator fragment, lane = 4 g + t): lane holds
+// rows g and g + 8 of its warp's 16 rows and columns 8 j + 2 t, 8 j + 2 t + 1
+// of every 8-column block j.  These are also the A fragments of MMA1 (the
+// pairs of an m16n8k16 A fragment), and after MMA1 lane t of a row quad owns
+// steps 2t, 2t+1, 8+2t, 9+2t -- exactly the A fragment of MMA2.
+//
+// Without folds the per-row solve is itself a small dense product: d_t =
+// beta_t (v_t / G'_t - a_t) gives (I + N) d = r with N[t][u] = beta_t
+// (k_u . k_t) for u < t and r_t = beta_t (v_t / G'_t - P_t), the same N for
+// every row.  The CTA inverts the unit lower-triangular 16 x 16 (I + N) once
+// per chunk (forward substitution, one lane per column) and every warp forms
+// D = R W^T and the corrected q dots B = PQ + D KQs^T with two more MMAs.
+//
+// A fold of the scale (G' out of range, see scale_in_range) at step f scales
+// the pending dots and the already computed d by G'_f and the chunk's state
+// by the product of the folds before MMA2; otherwise the semantics are those
+// of record.cuh.  Replay of a bf16 tape stays on the FP32 kernel.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "record.cuh"
+#include "tile.cuh"
+
+namespace gdn {
+
+constexpr int kMmaChunk = 16;                 // timesteps per chunk (one k16 tile of MMA2)
+constexpr int kMmaWarps = 4;                  // warps per CTA
+constexpr int kMmaRows = 16 * kMmaWarps;      // state rows per CTA
+constexpr int kKTStride = 24;                 // bf16 stride of a transposed k column (16 steps + pad)
+__host__ __device__ constexpr int mma_kstride(int dk) { return dk + 8; }  // padded bf16 k / q row
+
+__host__ __device__ constexpr bool record_mma_supported(int dk) { return dk == 64 || dk == 128; }
+
+constexpr int kWStride = 24;  // bf16 stride of the rows of W and KQs^T (16 + pad)
+
+// Shared memory (bytes), in carve order: ring 2 x {K[16][dk+8], Q[16][dk+8], V[16][64]} bf16;
+// KT[dk][24] bf16; KK, KQ [16][16] f32; W hi/lo, KQs^T hi/lo [16][24] bf16;
+// StepScalars[16]; g[16]; {direct bits, final scale}.
+__host__ __device__ constexpr size_t record_mma_smem_bytes(int dk) {
+    return 2 * align16((size_t)(2 * kMmaChunk * mma_kstride(dk) + kMmaChunk * kMmaRows) * 2) +
+           align16((size_t)dk * kKTStride * 2) + 2 * kMmaChunk * kMmaChunk * 4 +
+           4 * kMmaChunk * kWStride * 2 + align16(kMmaChunk * sizeof(StepScalars)) +
+           align16(kMmaChunk * 4) + 16;
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (x0, x1) ~ hi + lo with hi, lo packed bf16 pairs (x0 in the low half).
+// x - bf16(x) is exact in f32, so the pair carries 16 significant bits.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+__device__ __forceinline__ uint32_t lds32(const __nv_bfloat16 *p) {
+    return *reinterpret_cast<const uint32_t *>(p);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const RecordArgs a) {
+    using T = __nv_bfloat16;
+    constexpr int NT = DK / 8;   // 8-column blocks of a state row
+    constexpr int KT = DK / 16;  // k16 tiles along Dk
+    constexpr int KS = mma_kstride(DK);
+    constexpr int C = kMmaChunk;
+    constexpr int R = kMmaRows;
+    extern __shared__ __align__(16) unsigned char smem[];
+
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t n = blockIdx.x / a.row_blocks;
+    const int64_t rb = blockIdx.x - n * a.row_blocks;
+    const int64_t b = n / a.Hv, hv = n - b * a.Hv;
+    const int64_t hk = hv / (a.Hv / a.Hk);
+    const int64_t row0 = rb * R;
+    const int vlim = (int)min((int64_t)R, a.Dv - row0);
+    const int lr[2] = {warp * 16 + g, warp * 16 + g + 8};  // this lane's two local rows
+    const bool live0 = lr[0] < vlim, live1 = lr[1] < vlim;
+
+    // ---- shared memory
+    const size_t slot_bytes = align16((size_t)(2 * C * KS + C * R) * sizeof(T));
+    unsigned char *ring = smem;
+    auto slotK = [&](int sl) { return reinterpret_cast<T *>(ring + sl * slot_bytes); };
+    auto slotQ = [&](int sl) { return slotK(sl) + C * KS; };
+    auto slotV = [&](int sl) { return slotK(sl) + 2 * C * KS; };
+    unsigned char *p = ring + 2 * slot_bytes;
+    T *sKT = reinterpret_cast<T *>(p);
+    p += align16((size_t)DK * kKTStride * 2);
+    float *sKK = reinterpret_cast<float *>(p);
+    float *sKQ = sKK + C * C;
+    p += 2 * C * C * 4;
+    T *sWh = reinterpret_cast<T *>(p);       // W = (I + N)^-1, [t][u], hi / lo bf16 terms
+    T *sWl = sWh + C * kWStride;
+    T *sQh = sWl + C * kWStride;             // KQs^T[t][u] = k_u . q_t for u < t, hi / lo
+    T *sQl = sQh + C * kWStride;
+    p += 4 * C * kWStride * 2;
+    StepScalars *sc = reinterpret_cast<StepScalars *>(p);
+    p += align16(C * sizeof(StepScalars));
+    float *sg = reinterpret_cast<float *>(p);
+    p += align16(C * 4);
+    unsigned *s_direct = reinterpret_cast<unsigned *>(p);
+    float *s_gfinal = reinterpret_cast<float *>(p + 4);
+
+    const T *qp = static_cast<const T *>(a.q);
+    const T *kp = static_cast<const T *>(a.k);
+    const T *vp = static_cast<const T *>(a.v);
+    const T *gp = static_cast<const T *>(a.g);
+    const T *bp = static_cast<const T *>(a.beta);
+    T *yp = static_cast<T *>(a.y);
+    T *dp = static_cast<T *>(a.delta_log);
+    T *klp = static_cast<T *>(a.k_log);
+    T *glp = static_cast<T *>(a.g_log);
+    const bool capture = (rb == 0);
+
+    float pre_g = 1.f, pre_b = 0.f;
+    auto issue = [&](int64_t c) -> unsigned {
+        const int64_t t0 = c * C;
+        const int tcnt = (int)min((int64_t)C, a.T - t0);
+        const int slot = (int)(c & 1);
+        const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
+        const int64_t kq_off = ((b * a.T + t0) * a.Hk + hk) * DK;
+        async_rows_to<T>(slotK(slot), KS, kp + kq_off, a.Hk * DK, tcnt, DK, DK, bits, tid, nthr);
+        async_rows_to<T>(slotQ(slot), KS, qp + kq_off, a.Hk * DK, tcnt, DK, DK, bits, tid, nthr);
+        const int64_t v_off = ((b * a.T + t0) * a.Hv + hv) * a.Dv + row0;
+        if (a.vec_v) {
+            async_rows_to<T>(slotV(slot), R, vp + v_off, a.Hv * a.Dv, tcnt, R, vlim, bits, tid, nthr);
+        } else {
+            T *dst = slotV(slot);
+            for (int i = tid; i < tcnt * R; i += nthr) {
+                const int tt = i / R, r = i - tt * R;
+                if (((bits >> tt) & 1u) && r < vlim) dst[i] = vp[v_off + tt * a.Hv * a.Dv + r];
+            }
+        }
+        cp_async_commit();
+        if (tid < tcnt && ((bits >> tid) & 1u)) {
+            const int64_t gb = (b * a.T + t0 + tid) * a.Hv + hv;
+            pre_g = ld_f32(gp + gb);
+            pre_b = ld_f32(bp + gb);
+        }
+        return bits;
+    };
+
+    // ---- the state, as m16n8 accumulator fragments
+    unsigned next_bits = issue(0);
+    float st[NT][4];
+    {
+        const float2 *s0 = reinterpret_cast<const float2 *>(a.state_in + (n * a.Dv + row0 + lr[0]) * DK);
+        const float2 *s1 = reinterpret_cast<const float2 *>(a.state_in + (n * a.Dv + row0 + lr[1]) * DK);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const float2 x = live0 ? __ldcs(s0 + 4 * j + t) : make_float2(0.f, 0.f);
+            const float2 y = live1 ? __ldcs(s1 + 4 * j + t) : make_float2(0.f, 0.f);
+            st[j][0] = x.x;
+            st[j][1] = x.y;
+            st[j][2] = y.x;
+            st[j][3] = y.y;
+        }
+    }
+    float G_sched = 1.f;
+
+    const int64_t nchunks = (a.T + C - 1) / C;
+    for (int64_t c = 0; c < nchunks; ++c) {
+        const int64_t t0 = c * C;
+        const int tcnt = (int)min((int64_t)C, a.T - t0);
+        const int slot = (int)(c & 1);
+        const unsigned bits = next_bits;
+        cp_async_wait_all();
+        __syncthreads();  // (a) chunk c staged; chunk c-1 fully consumed
+        const T *cK = slotK(slot), *cQ = slotQ(slot), *cV = slotV(slot);
+        // k transposed (columns x steps) for MMA2; zero on inactive steps
+        for (int i = tid; i < DK * C; i += nthr) {
+            const int col = i >> 4, tt = i & (C - 1);
+            sKT[col * kKTStride + tt] = ((bits >> tt) & 1u) ? cK[tt * KS + col] : __float2bfloat16_rn(0.f);
+        }
+        if (tid < tcnt) {
+            sg[tid] = pre_g;
+            sc[tid].beta = pre_b;
+        }
+        if (capture) {
+            const int64_t gb0 = (b * a.T + t0) * a.Hv + hv;
+            if (klp) {
+                for (int i = tid; i < tcnt * (DK / 8); i += nthr) {
+                    const int tt = i / (DK / 8), x = (i - tt * (DK / 8)) * 8;
+                    if ((bits >> tt) & 1u)
+                        *reinterpret_cast<uint4 *>(klp + (gb0 + tt * a.Hv) * DK + x) =
+                            *reinterpret_cast<const uint4 *>(cK + tt * KS + x);
+                }
+            }
+            if (glp && tid < tcnt && ((bits >> tid) & 1u)) st_from_f32(glp + gb0 + tid * a.Hv, pre_g);
+        }
+        __syncthreads();  // (b)
+        if (c + 1 < nchunks) next_bits = issue(c + 1);
+        if (warp == 0) {
+            // Gram matrices of the chunk: KK[u][s] = k_u . k_s, KQ[u][s] = k_u . q_s
+            float kk[2][4] = {}, kq[2][4] = {};
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt) {
+                const uint32_t af[4] = {lds32(cK + g * KS + 16 * kt + 2 * t),
+                                        lds32(cK + (g + 8) * KS + 16 * kt + 2 * t),
+                                        lds32(cK + g * KS + 16 * kt + 2 * t + 8),
+                                        lds32(cK + (g + 8) * KS + 16 * kt + 2 * t + 8)};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const T *kr = cK + (8 * nt + g) * KS + 16 * kt + 2 * t;
+                    const T *qr = cQ + (8 * nt + g) * KS + 16 * kt + 2 * t;
+                    mma_bf16_16816(kk[nt], af, lds32(kr), lds32(kr + 8));
+                    mma_bf16_16816(kq[nt], af, lds32(qr), lds32(qr + 8));
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int u = g + 8 * (e >> 1), s2 = 8 * nt + 2 * t + (e & 1);
+                    // entries that involve a masked / absent step are exact zeros
+                    // (their staged rows are stale and may hold anything)
+                    const bool on = s2 > u && ((bits >> u) & 1u) && ((bits >> s2) & 1u);
+                    sKK[u * C + s2] = on ? kk[nt][e] : 0.f;
+                    sKQ[u * C + s2] = on ? kq[nt][e] : 0.f;
+                    if (s2 == u) sc[u].kq = kq[nt][e];
+                }
+        }
+        if (warp == (nthr >> 5) - 1) {
+            const unsigned dbits = scale_schedule(sc, sg, bits, tcnt, G_sched, lane);
+            if (lane == 0) {
+                *s_direct = dbits;
+                *s_gfinal = G_sched;
+            }
+        }
+        __syncthreads();  // (c) Gram matrices and per-step scalars ready
+        const unsigned direct = *s_direct;
+
+        if (warp == 1 && direct == 0u) {
+            if (lane < C) {
+                // column u = lane of W = (I + N)^-1 by forward substitution,
+                // N[t][s] = beta_t KK[s][t] (zero unless s < t, both active)
+                const int u = lane;
+                float w[C];
+#pragma unroll
+                for (int t2 = 0; t2 < C; ++t2) {
+                    float acc2 = 0.f;
+                    const float bt = ((bits >> t2) & 1u) ? sc[t2].beta : 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < t2; ++s2) acc2 = fmaf(sKK[s2 * C + t2], w[s2], acc2);
+                    w[t2] = t2 < u ? 0.f : (t2 == u ? 1.f : -bt * acc2);
+                }
+#pragma unroll
+                for (int t2 = 0; t2 < C; ++t2) {
+                    const __nv_bfloat16 h = __float2bfloat16_rn(w[t2]);
+                    sWh[t2 * kWStride + u] = h;
+                    sWl[t2 * kWStride + u] = __float2bfloat16_rn(w[t2] - __bfloat162float(h));
+                }
+            } else {
+                // KQs^T[t][u] = KQ[u][t] (already zero unless u < t, both active)
+                const int t2 = lane - C;
+#pragma unroll
+                for (int u = 0; u < C; ++u) {
+                    const float x = sKQ[u * C + t2];
+                    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+                    sQh[t2 * kWStride + u] = h;
+                    sQl[t2 * kWStride + u] = __float2bfloat16_rn(x - __bfloat162float(h));
+                }
+            }
+        }
+
+        // ---- MMA1: the chunk's step dots from the chunk-initial state
+        float acc[4][4] = {};  // [k steps 0-7, k steps 8-15, q steps 0-7, q steps 8-15]
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+            uint32_t ah[4], al[4];
+            split_bf16x2(st[2 * kt][0], st[2 * kt][1], ah[0], al[0]);
+            split_bf16x2(st[2 * kt][2], st[2 * kt][3], ah[1], al[1]);
+            split_bf16x2(st[2 * kt + 1][0], st[2 * kt + 1][1], ah[2], al[2]);
+            split_bf16x2(st[2 * kt + 1][2], st[2 * kt + 1][3], ah[3], al[3]);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const T *rowp = (nt < 2 ? cK : cQ) + ((nt & 1) * 8 + g) * KS + 16 * kt + 2 * t;
+                const uint32_t b0 = lds32(rowp), b1 = lds32(rowp + 8);
+                mma_bf16_16816(acc[nt], ah, b0, b1);
+                mma_bf16_16816(acc[nt], al, b0, b1);
+            }
+        }
+        __syncthreads();  // (d) W and KQs^T ready
+
+        // ---- the per-row solve.  Lane t of a quad holds steps {2t, 2t+1,
+        // 8+2t, 9+2t} (index [hi][lo]) of rows lr[0], lr[1] (index r).
+        float d[2][2][2];
+        float phi_all = 1.f;
+        if (direct == 0u) {
+            // r_t = beta_t (v_t / G'_t - P_t);  D = R W^T;  B = PQ + D KQs^T
+            StepScalars S4[2][2];
+            float r[2][2][2];
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+                for (int lo = 0; lo < 2; ++lo) {
+                    const int stp = 8 * hi + 2 * t + lo;
+                    S4[hi][lo] = sc[stp];
+                    const bool on = (bits >> stp) & 1u;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const float vval = __bfloat162float(cV[stp * R + lr[rr]]);
+                        r[hi][lo][rr] =
+                            on ? S4[hi][lo].beta * (vval * S4[hi][lo].inv - acc[hi][2 * rr + lo]) : 0.f;
+                    }
+                }
+            uint32_t rh[4], rl[4];
+            split_bf16x2(r[0][0][0], r[0][1][0], rh[0], rl[0]);
+            split_bf16x2(r[0][0][1], r[0][1][1], rh[1], rl[1]);
+            split_bf16x2(r[1][0][0], r[1][1][0], rh[2], rl[2]);
+            split_bf16x2(r[1][0][1], r[1][1][1], rh[3], rl[3]);
+            float dacc[2][4] = {};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int off = (8 * nt + g) * kWStride + 2 * t;
+                const uint32_t wh0 = lds32(sWh + off), wh1 = lds32(sWh + off + 8);
+                const uint32_t wl0 = lds32(sWl + off), wl1 = lds32(sWl + off + 8);
+                mma_bf16_16816(dacc[nt], rh, wh0, wh1);
+                mma_bf16_16816(dacc[nt], rh, wl0, wl1);
+                mma_bf16_16816(dacc[nt], rl, wh0, wh1);
+            }
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+                for (int lo = 0; lo < 2; ++lo)
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) d[hi][lo][rr] = dacc[hi][2 * rr + lo];
+            uint32_t dh[4], dl[4];
+            split_bf16x2(d[0][0][0], d[0][1][0], dh[0], dl[0]);
+            split_bf16x2(d[0][0][1], d[0][1][1], dh[1], dl[1]);
+            split_bf16x2(d[1][0][0], d[1][1][0], dh[2], dl[2]);
+            split_bf16x2(d[1][0][1], d[1][1][1], dh[3], dl[3]);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int off = (8 * nt + g) * kWStride + 2 * t;
+                const uint32_t qh0 = lds32(sQh + off), qh1 = lds32(sQh + off + 8);
+                const uint32_t ql0 = lds32(sQl + off), ql1 = lds32(sQl + off + 8);
+                mma_bf16_16816(acc[2 + nt], dh, qh0, qh1);
+                mma_bf16_16816(acc[2 + nt], dh, ql0, ql1);
+                mma_bf16_16816(acc[2 + nt], dl, qh0, qh1);
+            }
+            // outputs: delta = G' d, y = G' b + delta (k.q)
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+                for (int lo = 0; lo < 2; ++lo) {
+                    const int stp = 8 * hi + 2 * t + lo;
+                    if (!((bits >> stp) & 1u)) continue;
+                    const StepScalars &S = S4[hi][lo];
+                    const int64_t o = ((b * a.T + t0 + stp) * a.Hv + hv) * a.Dv + row0;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        if (!(rr == 0 ? live0 : live1)) continue;
+                        const float delta = S.Gp * d[hi][lo][rr];
+                        const float yv = fmaf(S.Gp, acc[2 + hi][2 * rr + lo], delta * S.kq);
+                        st_from_f32(yp + o + lr[rr], yv);
+                        st_from_f32(dp + o + lr[rr], delta);
+                    }
+                }
+        } else {
+            // a fold of the scale inside the chunk: the serial solve
+            float pa[2][2][2], pb[2][2][2], vv[2][2][2];
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+                for (int lo = 0; lo < 2; ++lo)
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        pa[hi][lo][rr] = acc[hi][2 * rr + lo];
+                        pb[hi][lo][rr] = acc[2 + hi][2 * rr + lo];
+                        vv[hi][lo][rr] = __bfloat162float(cV[(8 * hi + 2 * t + lo) * R + lr[rr]]);
+                        d[hi][lo][rr] = 0.f;
+                    }
+            const int qbase = lane & ~3;
+            for (int tau = 0; tau < C; ++tau) {
+                if (!((bits >> tau) & 1u)) continue;  // uniform across the CTA
+                const StepScalars S = sc[tau];
+                const bool fold = (direct >> tau) & 1u;
+                if (fold) {  // s^ <- G' s^ before this step: rescale what depends on s^
+                    const float phi = S.Gp;
+                    phi_all *= phi;
+#pragma unroll
+                    for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+                        for (int lo = 0; lo < 2; ++lo)
+#pragma unroll
+                            for (int rr = 0; rr < 2; ++rr) {
+                                pa[hi][lo][rr] *= phi;
+                                pb[hi][lo][rr] *= phi;
+                                d[hi][lo][rr] *= phi;
+                            }
+                }
+                const float Gp = fold ? 1.f : S.Gp;
+                const int HI = tau >> 3, LO = tau & 1, TO = (tau & 7) >> 1;
+                float dn[2];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    // select the owner's slot with compile-time indices
+                    float pav = 0.f, pbv = 0.f, vvv = 0.f;
+#pragma unroll
+                    for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+                        for (int lo = 0; lo < 2; ++lo)
+                            if (hi == HI && lo == LO) {
+                                pav = pa[hi][lo][rr];
+                                pbv = pb[hi][lo][rr];
+                                vvv = vv[hi][lo][rr];
+                            }
+                    const float kv = Gp * pav;
+                    const float delta = (vvv - kv) * S.beta;
+                    const float yv = fmaf(Gp, pbv, delta * S.kq);
+                    const float dd = delta * S.inv;
+                    if (t == TO) {
+#pragma unroll
+                        for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+                            for (int lo = 0; lo < 2; ++lo)
+                                if (hi == HI && lo == LO) d[hi][lo][rr] = dd;
+                        if (rr == 0 ? live0 : live1) {
+                            const int64_t o = ((b * a.T + t0 + tau) * a.Hv + hv) * a.Dv + row0;
+                            st_from_f32(yp + o + lr[rr], yv);
+                            st_from_f32(dp + o + lr[rr], delta);
+                        }
+                    }
+                    dn[rr] = __shfl_sync(0xffffffffu, dd, qbase + TO);
+                }
+                const float2 k0 = *reinterpret_cast<const float2 *>(sKK + tau * C + 2 * t);
+                const float2 k1 = *reinterpret_cast<const float2 *>(sKK + tau * C + 8 + 2 * t);
+                const float2 q0 = *reinterpret_cast<const float2 *>(sKQ + tau * C + 2 * t);
+                const float2 q1 = *reinterpret_cast<const float2 *>(sKQ + tau * C + 8 + 2 * t);
+                const float kc[2][2] = {{k0.x, k0.y}, {k1.x, k1.y}};
+                const float qc[2][2] = {{q0.x, q0.y}, {q1.x, q1.y}};
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+                    for (int lo = 0; lo < 2; ++lo)
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            pa[hi][lo][rr] = fmaf(dn[rr], kc[hi][lo], pa[hi][lo][rr]);
+                            pb[hi][lo][rr] = fmaf(dn[rr], qc[hi][lo], pb[hi][lo][rr]);
+                        }
+            }
+        }
+
+        // ---- MMA2: s^ += D K over the chunk's steps
+        if (phi_all != 1.f) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) st[j][e] *= phi_all;
+        }
+        uint32_t dh[4], dl[4];
+        split_bf16x2(d[0][0][0], d[0][1][0], dh[0], dl[0]);
+        split_bf16x2(d[0][0][1], d[0][1][1], dh[1], dl[1]);
+        split_bf16x2(d[1][0][0], d[1][1][0], dh[2], dl[2]);
+        split_bf16x2(d[1][0][1], d[1][1][1], dh[3], dl[3]);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const T *kc = sKT + (8 * j + g) * kKTStride + 2 * t;
+            const uint32_t b0 = lds32(kc), b1 = lds32(kc + 8);
+            mma_bf16_16816(st[j], dh, b0, b1);
+            mma_bf16_16816(st[j], dl, b0, b1);
+        }
+    }
+
+    // ---- s = G s^, streaming stores
+    const float G = nchunks > 0 ? *s_gfinal : 1.f;
+    float2 *o0 = reinterpret_cast<float2 *>(a.state_out + (n * a.Dv + row0 + lr[0]) * DK);
+    float2 *o1 = reinterpret_cast<float2 *>(a.state_out + (n * a.Dv + row0 + lr[1]) * DK);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        if (live0) __stcs(o0 + 4 * j + t, make_float2(st[j][0] * G, st[j][1] * G));
+        if (live1) __stcs(o1 + 4 * j + t, make_float2(st[j][2] * G, st[j][3] * G));
+    }
+}
+
+template <int DK>
+cudaError_t launch_record_mma(const RecordArgs &a, const Geometry &geo, cudaStream_t st) {
+    auto kern = record_mma_kernel<DK>;
+    if (geo.smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)geo.smem);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t blocks = (int64_t)(a.B * a.Hv) * geo.row_blocks;
+    kern<<<(unsigned)blocks, geo.threads, geo.smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

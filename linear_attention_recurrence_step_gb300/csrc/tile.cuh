@@ -61,15 +61,14 @@ __device__ __forceinline__ int64_t row_base4(int64_t n, int64_t Dv, int64_t dv, 
     return ((n * Dv + dv) * dk) >> 2;
 }
 
-// Load this thread's rows of the tile (zeros for rows past Dv).  Register
-// slot m holds row row_first + (m ^ perm).
+// Load this thread's rows of the tile (zeros for rows past Dv).
 template <class Lay>
 __device__ __forceinline__ void load_rows(Slice<Lay> &s, const float *state, int64_t n, int64_t Dv,
-                                          int64_t row_first, int j, int perm = 0) {
+                                          int64_t row_first, int j) {
     const float4 *p = reinterpret_cast<const float4 *>(state);
 #pragma unroll
     for (int m = 0; m < Lay::RT; ++m) {
-        const int64_t dv = row_first + (m ^ perm);
+        const int64_t dv = row_first + m;
         const bool live = dv < Dv;
         const int64_t base = live ? row_base4(n, Dv, dv, Lay::DK) : 0;
 #pragma unroll
@@ -81,13 +80,13 @@ __device__ __forceinline__ void load_rows(Slice<Lay> &s, const float *state, int
 // s <- s * G for the whole slice, then store rows < Dv (streaming stores).
 template <class Lay>
 __device__ __forceinline__ void store_rows(Slice<Lay> &s, float G, float *state, int64_t n,
-                                           int64_t Dv, int64_t row_first, int j, int perm = 0) {
+                                           int64_t Dv, int64_t row_first, int j) {
     float4 *p = reinterpret_cast<float4 *>(state);
     const float2 g2 = make_float2(G, G);
     const bool scale = G != 1.f;
 #pragma unroll
     for (int m = 0; m < Lay::RT; ++m) {
-        const int64_t dv = row_first + (m ^ perm);
+        const int64_t dv = row_first + m;
         if (dv >= Dv) continue;
         const int64_t base = row_base4(n, Dv, dv, Lay::DK);
 #pragma unroll
@@ -132,27 +131,26 @@ __device__ __forceinline__ void lane_chunks(float4 (&out)[Lay::NCH], const float
     for (int c = 0; c < Lay::NCH; ++c) out[c] = r4[c * Lay::L + j];
 }
 
-// Transposed butterfly over the L lanes of a row group, without selects.
-// The record kernel stores its rows permuted per lane -- register slot m of
-// lane j holds row m ^ row_perm(j) -- and, when two lanes share a row
-// (REDV == 1), odd lanes accumulate the q dot in the first slot of a pair.
-// With that layout, value slot u of lane j holds list entry u ^ j of the
-// list [a_0, b_0, a_1, b_1, ...] (REDV == 1) or row slot m holds row m ^ j
-// (REDV == 2), so every level is "keep the lower half, add the partner's
-// upper half": at offset o the partner's slot u + o holds exactly the entry
-// of my slot u.  On exit slot 0 (REDV == 1) or slots 0, 1 (REDV == 2) hold
-// the group sums for list entry j (row j / 2, dot j % 2) or row j.
+// Transposed butterfly over the L lanes of a row group: on entry v[2m],
+// v[2m+1] are this lane's partial (s.k, s.q) of row m; on exit v[0 .. REDV)
+// holds the group sums of entries [REDV * j, REDV * j + REDV) of that list.
+// Each level halves the list: lanes with the level's bit set keep the upper
+// half.  (Keeping the rows in natural order keeps the one-time state
+// load / store coalesced; a per-lane row permutation would remove the
+// selects but splits every 128-byte line across eight rows.)
 template <class Lay>
-__device__ __forceinline__ int row_perm(int j) { return Lay::REDV == 2 ? j : (j >> 1); }
-
-template <class Lay>
-__device__ __forceinline__ void transpose_reduce(float (&v)[2 * Lay::RT]) {
+__device__ __forceinline__ void transpose_reduce(float (&v)[2 * Lay::RT], int j) {
 #pragma unroll
     for (int lvl = 0; lvl < Lay::LOG2L; ++lvl) {
-        const int o = Lay::L >> (lvl + 1);       // lane offset of this level
-        const int w = Lay::REDV == 2 ? 2 : 1;    // list entries per slot unit
+        const int o = Lay::L >> (lvl + 1);
+        const int half = (2 * Lay::RT) >> (lvl + 1);
+        const bool upper = (j & o) != 0;
 #pragma unroll
-        for (int i = 0; i < o * w; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + o * w], o);
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
     }
 }
 
@@ -226,6 +224,21 @@ __device__ __forceinline__ void async_rows(T *dst, const T *src, int64_t stride,
         const int tt = i / vpr;
         const int x = (i - tt * vpr) * VEC;
         if (((bits >> tt) & 1u) && x < limit) cp_async16(dst + tt * row_elems + x, src + tt * stride + x);
+    }
+}
+
+// As async_rows, with a destination row stride (elements) that may differ
+// from the row length (padded shared-memory rows).
+template <typename T>
+__device__ __forceinline__ void async_rows_to(T *dst, int dst_stride, const T *src, int64_t stride,
+                                              int tcnt, int row_elems, int limit, unsigned bits,
+                                              int tid, int nthr) {
+    constexpr int VEC = 16 / sizeof(T);
+    const int vpr = row_elems / VEC;
+    for (int i = tid; i < tcnt * vpr; i += nthr) {
+        const int tt = i / vpr;
+        const int x = (i - tt * vpr) * VEC;
+        if (((bits >> tt) & 1u) && x < limit) cp_async16(dst + tt * dst_stride + x, src + tt * stride + x);
     }
 }
 

@@ -201,6 +201,20 @@ def test_decay_edges(dev):
         assert torch.equal(st, got["state_out"]), f"bit-exact replay, seed {seed}"
 
 
+@pytest.mark.parametrize("Dk", [64, 128])
+def test_decay_edges_bf16_chunked(dev, Dk):
+    """bf16 inputs with T >= 12 take the tensor-core chunk kernel: g = 0,
+    scale folds inside chunks (products of g below 2^-32), masks and a
+    ragged last chunk."""
+    for seed, T, g_range, mask in [(5, 16, (0.0, 0.0), "none"), (6, 80, (0.3, 0.5), "bernoulli:0.7"),
+                                   (7, 45, (0.9, 1.0), "bernoulli:0.5"), (8, 37, (0.6, 1.0), "prefix")]:
+        case = workloads.make_case(B=2, T=T, Hk=2, Hv=4, Dk=Dk, Dv=72, dtype="bf16", seed=seed,
+                                   g_range=g_range, mask=mask)
+        got, s0, m = _run_record(case, dev)
+        ref = oracle.record(*_oracle_inputs(case))
+        _check_record(case, got, ref)
+
+
 def test_growth_past_scale_limit(dev):
     """g in (2, 3) for 36 steps: the scale product passes 2^32 and states reach
     ~1e13.  Under growth, f32 carries absolute error proportional to each
