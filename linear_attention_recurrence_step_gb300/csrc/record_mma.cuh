@@ -51,21 +51,20 @@ namespace gdn {
 constexpr int kMmaChunk = 16;                 // timesteps per chunk (one k16 tile of MMA2)
 constexpr int kMmaWarps = 4;                  // warps per CTA
 constexpr int kMmaRows = 16 * kMmaWarps;      // state rows per CTA
-constexpr int kKTStride = 24;                 // bf16 stride of a transposed k column (16 steps + pad)
+constexpr int kWStride = 24;                  // bf16 stride of the rows of W and KQs^T (16 + pad)
 __host__ __device__ constexpr int mma_kstride(int dk) { return dk + 8; }  // padded bf16 k / q row
 
 __host__ __device__ constexpr bool record_mma_supported(int dk) { return dk == 64 || dk == 128; }
 
-constexpr int kWStride = 24;  // bf16 stride of the rows of W and KQs^T (16 + pad)
-
-// Shared memory (bytes), in carve order: ring 2 x {K[16][dk+8], Q[16][dk+8], V[16][64]} bf16;
-// KT[dk][24] bf16; KK, KQ [16][16] f32; W hi/lo, KQs^T hi/lo [16][24] bf16;
-// StepScalars[16]; g[16]; {direct bits, final scale}.
+// Shared memory (bytes), in carve order:
+//   ring     2 x { K[16][dk+8], Q[16][dk+8], V[16][64] }  bf16
+//   KK, KQ   [16][16] f32
+//   W hi/lo, KQs^T hi/lo   [16][24] bf16
+//   scalars  2 x { StepScalars[16], g[16] }, {direct bits, final scale}
 __host__ __device__ constexpr size_t record_mma_smem_bytes(int dk) {
     return 2 * align16((size_t)(2 * kMmaChunk * mma_kstride(dk) + kMmaChunk * kMmaRows) * 2) +
-           align16((size_t)dk * kKTStride * 2) + 2 * kMmaChunk * kMmaChunk * 4 +
-           4 * kMmaChunk * kWStride * 2 + align16(kMmaChunk * sizeof(StepScalars)) +
-           align16(kMmaChunk * 4) + 16;
+           2 * kMmaChunk * kMmaChunk * 4 + 4 * kMmaChunk * kWStride * 2 +
+           2 * (align16(kMmaChunk * sizeof(StepScalars)) + align16(kMmaChunk * 4)) + 16;
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -75,6 +74,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 bf16 matrices from shared memory; lane l gives the address of row
+// l % 8 of matrix l / 8.  Plain: lane (g, t) receives (row g, cols 2t, 2t+1)
+// of each matrix; .trans: (rows 2t, 2t+1, col g).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *row) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(row));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *row) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(row));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
 }
 
 // (x0, x1) ~ hi + lo with hi, lo packed bf16 pairs (x0 in the low half).
@@ -104,6 +119,7 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
+    const int lm = lane >> 3, lr8 = lane & 7;  // ldmatrix: matrix and row this lane addresses
     const int64_t n = blockIdx.x / a.row_blocks;
     const int64_t rb = blockIdx.x - n * a.row_blocks;
     const int64_t b = n / a.Hv, hv = n - b * a.Hv;
@@ -120,22 +136,21 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
     auto slotQ = [&](int sl) { return slotK(sl) + C * KS; };
     auto slotV = [&](int sl) { return slotK(sl) + 2 * C * KS; };
     unsigned char *p = ring + 2 * slot_bytes;
-    T *sKT = reinterpret_cast<T *>(p);
-    p += align16((size_t)DK * kKTStride * 2);
     float *sKK = reinterpret_cast<float *>(p);
     float *sKQ = sKK + C * C;
     p += 2 * C * C * 4;
-    T *sWh = reinterpret_cast<T *>(p);       // W = (I + N)^-1, [t][u], hi / lo bf16 terms
+    T *sWh = reinterpret_cast<T *>(p);  // W = (I + N)^-1, [t][u], hi / lo bf16 terms
     T *sWl = sWh + C * kWStride;
-    T *sQh = sWl + C * kWStride;             // KQs^T[t][u] = k_u . q_t for u < t, hi / lo
+    T *sQh = sWl + C * kWStride;        // KQs^T[t][u] = k_u . q_t for u < t, hi / lo
     T *sQl = sQh + C * kWStride;
     p += 4 * C * kWStride * 2;
-    StepScalars *sc = reinterpret_cast<StepScalars *>(p);
-    p += align16(C * sizeof(StepScalars));
-    float *sg = reinterpret_cast<float *>(p);
-    p += align16(C * 4);
-    unsigned *s_direct = reinterpret_cast<unsigned *>(p);
-    float *s_gfinal = reinterpret_cast<float *>(p + 4);
+    const size_t sc_set = align16(C * sizeof(StepScalars)) + align16(C * 4);
+    auto scS = [&](int set) { return reinterpret_cast<StepScalars *>(p + set * sc_set); };
+    auto sgS = [&](int set) {
+        return reinterpret_cast<float *>(p + set * sc_set + align16(C * sizeof(StepScalars)));
+    };
+    unsigned *s_direct = reinterpret_cast<unsigned *>(p + 2 * sc_set);
+    float *s_gfinal = reinterpret_cast<float *>(p + 2 * sc_set + 4);
 
     const T *qp = static_cast<const T *>(a.q);
     const T *kp = static_cast<const T *>(a.k);
@@ -148,12 +163,24 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
     T *glp = static_cast<T *>(a.g_log);
     const bool capture = (rb == 0);
 
+    // ---- issue chunk c into ring slot c & 1.  Rows of inactive steps (masked,
+    // or past the end of the call) are zeroed: MMA2 multiplies every row of
+    // the chunk, and a stale row could hold NaN.
     float pre_g = 1.f, pre_b = 0.f;
     auto issue = [&](int64_t c) -> unsigned {
         const int64_t t0 = c * C;
         const int tcnt = (int)min((int64_t)C, a.T - t0);
         const int slot = (int)(c & 1);
         const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
+        if (bits != 0xffffu) {
+            for (int i = tid; i < C * (DK / 8); i += nthr) {
+                const int tt = i / (DK / 8), x = (i - tt * (DK / 8)) * 8;
+                if (!((bits >> tt) & 1u)) {
+                    *reinterpret_cast<uint4 *>(slotK(slot) + tt * KS + x) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(slotQ(slot) + tt * KS + x) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
         const int64_t kq_off = ((b * a.T + t0) * a.Hk + hk) * DK;
         async_rows_to<T>(slotK(slot), KS, kp + kq_off, a.Hk * DK, tcnt, DK, DK, bits, tid, nthr);
         async_rows_to<T>(slotQ(slot), KS, qp + kq_off, a.Hk * DK, tcnt, DK, DK, bits, tid, nthr);
@@ -198,21 +225,20 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
     for (int64_t c = 0; c < nchunks; ++c) {
         const int64_t t0 = c * C;
         const int tcnt = (int)min((int64_t)C, a.T - t0);
-        const int slot = (int)(c & 1);
+        const int slot = (int)(c & 1), set = (int)(c & 1);
         const unsigned bits = next_bits;
-        cp_async_wait_all();
-        __syncthreads();  // (a) chunk c staged; chunk c-1 fully consumed
-        const T *cK = slotK(slot), *cQ = slotQ(slot), *cV = slotV(slot);
-        // k transposed (columns x steps) for MMA2; zero on inactive steps
-        for (int i = tid; i < DK * C; i += nthr) {
-            const int col = i >> 4, tt = i & (C - 1);
-            sKT[col * kKTStride + tt] = ((bits >> tt) & 1u) ? cK[tt * KS + col] : __float2bfloat16_rn(0.f);
-        }
-        if (tid < tcnt) {
+        StepScalars *sc = scS(set);
+        float *sg = sgS(set);
+        if (tid < tcnt) {  // this set was last read two chunks ago
             sg[tid] = pre_g;
             sc[tid].beta = pre_b;
         }
-        if (capture) {
+        cp_async_wait_all();
+        __syncthreads();  // (a) chunk c staged and its scalars visible; chunk c-1 fully consumed
+        if (c + 1 < nchunks) next_bits = issue(c + 1);
+        const T *cK = slotK(slot), *cQ = slotQ(slot), *cV = slotV(slot);
+
+        if (capture) {  // tape capture: k_log / g_log rows of the active steps
             const int64_t gb0 = (b * a.T + t0) * a.Hv + hv;
             if (klp) {
                 for (int i = tid; i < tcnt * (DK / 8); i += nthr) {
@@ -222,26 +248,22 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
                             *reinterpret_cast<const uint4 *>(cK + tt * KS + x);
                 }
             }
-            if (glp && tid < tcnt && ((bits >> tid) & 1u)) st_from_f32(glp + gb0 + tid * a.Hv, pre_g);
+            if (glp && tid < tcnt && ((bits >> tid) & 1u)) st_from_f32(glp + gb0 + tid * a.Hv, sg[tid]);
         }
-        __syncthreads();  // (b)
-        if (c + 1 < nchunks) next_bits = issue(c + 1);
+
         if (warp == 0) {
-            // Gram matrices of the chunk: KK[u][s] = k_u . k_s, KQ[u][s] = k_u . q_s
+            // Gram matrices KK[u][s] = k_u . k_s, KQ[u][s] = k_u . q_s (one warp)
             float kk[2][4] = {}, kq[2][4] = {};
 #pragma unroll
             for (int kt = 0; kt < KT; ++kt) {
-                const uint32_t af[4] = {lds32(cK + g * KS + 16 * kt + 2 * t),
-                                        lds32(cK + (g + 8) * KS + 16 * kt + 2 * t),
-                                        lds32(cK + g * KS + 16 * kt + 2 * t + 8),
-                                        lds32(cK + (g + 8) * KS + 16 * kt + 2 * t + 8)};
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const T *kr = cK + (8 * nt + g) * KS + 16 * kt + 2 * t;
-                    const T *qr = cQ + (8 * nt + g) * KS + 16 * kt + 2 * t;
-                    mma_bf16_16816(kk[nt], af, lds32(kr), lds32(kr + 8));
-                    mma_bf16_16816(kq[nt], af, lds32(qr), lds32(qr + 8));
-                }
+                uint32_t ka[4], qa[4];
+                // matrices: (steps 0-7, k lo), (steps 8-15, k lo), (0-7, k hi), (8-15, k hi)
+                ldsm_x4(ka, cK + (lr8 + 8 * (lm & 1)) * KS + 16 * kt + 8 * (lm >> 1));
+                ldsm_x4(qa, cQ + (lr8 + 8 * (lm & 1)) * KS + 16 * kt + 8 * (lm >> 1));
+                mma_bf16_16816(kk[0], ka, ka[0], ka[2]);
+                mma_bf16_16816(kk[1], ka, ka[1], ka[3]);
+                mma_bf16_16816(kq[0], ka, qa[0], qa[2]);
+                mma_bf16_16816(kq[1], ka, qa[1], qa[3]);
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -249,24 +271,12 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
                 for (int e = 0; e < 4; ++e) {
                     const int u = g + 8 * (e >> 1), s2 = 8 * nt + 2 * t + (e & 1);
                     // entries that involve a masked / absent step are exact zeros
-                    // (their staged rows are stale and may hold anything)
                     const bool on = s2 > u && ((bits >> u) & 1u) && ((bits >> s2) & 1u);
                     sKK[u * C + s2] = on ? kk[nt][e] : 0.f;
                     sKQ[u * C + s2] = on ? kq[nt][e] : 0.f;
                     if (s2 == u) sc[u].kq = kq[nt][e];
                 }
-        }
-        if (warp == (nthr >> 5) - 1) {
-            const unsigned dbits = scale_schedule(sc, sg, bits, tcnt, G_sched, lane);
-            if (lane == 0) {
-                *s_direct = dbits;
-                *s_gfinal = G_sched;
-            }
-        }
-        __syncthreads();  // (c) Gram matrices and per-step scalars ready
-        const unsigned direct = *s_direct;
-
-        if (warp == 1 && direct == 0u) {
+            __syncwarp();
             if (lane < C) {
                 // column u = lane of W = (I + N)^-1 by forward substitution,
                 // N[t][s] = beta_t KK[s][t] (zero unless s < t, both active)
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
                 }
 #pragma unroll
                 for (int t2 = 0; t2 < C; ++t2) {
-                    const __nv_bfloat16 h = __float2bfloat16_rn(w[t2]);
+                    const T h = __float2bfloat16_rn(w[t2]);
                     sWh[t2 * kWStride + u] = h;
                     sWl[t2 * kWStride + u] = __float2bfloat16_rn(w[t2] - __bfloat162float(h));
                 }
@@ -292,10 +302,17 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
 #pragma unroll
                 for (int u = 0; u < C; ++u) {
                     const float x = sKQ[u * C + t2];
-                    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+                    const T h = __float2bfloat16_rn(x);
                     sQh[t2 * kWStride + u] = h;
                     sQl[t2 * kWStride + u] = __float2bfloat16_rn(x - __bfloat162float(h));
                 }
+            }
+        }
+        if (warp == kMmaWarps - 1) {
+            const unsigned dbits = scale_schedule(sc, sg, bits, tcnt, G_sched, lane);
+            if (lane == 0) {
+                *s_direct = dbits;
+                *s_gfinal = G_sched;
             }
         }
 
@@ -308,15 +325,21 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
             split_bf16x2(st[2 * kt][2], st[2 * kt][3], ah[1], al[1]);
             split_bf16x2(st[2 * kt + 1][0], st[2 * kt + 1][1], ah[2], al[2]);
             split_bf16x2(st[2 * kt + 1][2], st[2 * kt + 1][3], ah[3], al[3]);
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const T *rowp = (nt < 2 ? cK : cQ) + ((nt & 1) * 8 + g) * KS + 16 * kt + 2 * t;
-                const uint32_t b0 = lds32(rowp), b1 = lds32(rowp + 8);
-                mma_bf16_16816(acc[nt], ah, b0, b1);
-                mma_bf16_16816(acc[nt], al, b0, b1);
-            }
+            uint32_t kb[4], qb[4];
+            // matrices: (steps 0-7, k lo), (steps 0-7, k hi), (8-15, k lo), (8-15, k hi)
+            ldsm_x4(kb, cK + (lr8 + 8 * (lm >> 1)) * KS + 16 * kt + 8 * (lm & 1));
+            ldsm_x4(qb, cQ + (lr8 + 8 * (lm >> 1)) * KS + 16 * kt + 8 * (lm & 1));
+            mma_bf16_16816(acc[0], ah, kb[0], kb[1]);
+            mma_bf16_16816(acc[0], al, kb[0], kb[1]);
+            mma_bf16_16816(acc[1], ah, kb[2], kb[3]);
+            mma_bf16_16816(acc[1], al, kb[2], kb[3]);
+            mma_bf16_16816(acc[2], ah, qb[0], qb[1]);
+            mma_bf16_16816(acc[2], al, qb[0], qb[1]);
+            mma_bf16_16816(acc[3], ah, qb[2], qb[3]);
+            mma_bf16_16816(acc[3], al, qb[2], qb[3]);
         }
-        __syncthreads();  // (d) W and KQs^T ready
+        __syncthreads();  // (b) Gram matrices, W, KQs^T and per-step scalars ready
+        const unsigned direct = *s_direct;
 
         // ---- the per-row solve.  Lane t of a quad holds steps {2t, 2t+1,
         // 8+2t, 9+2t} (index [hi][lo]) of rows lr[0], lr[1] (index r).
@@ -478,7 +501,8 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
             }
         }
 
-        // ---- MMA2: s^ += D K over the chunk's steps
+        // ---- MMA2: s^ += D K over the chunk's steps (B fragments by ldmatrix.trans
+        // from the row-major k rows: matrices (steps 0-7 | 8-15) x (columns j | j+1))
         if (phi_all != 1.f) {
 #pragma unroll
             for (int j = 0; j < NT; ++j)
@@ -491,11 +515,13 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const Rec
         split_bf16x2(d[1][0][0], d[1][1][0], dh[2], dl[2]);
         split_bf16x2(d[1][0][1], d[1][1][1], dh[3], dl[3]);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const T *kc = sKT + (8 * j + g) * kKTStride + 2 * t;
-            const uint32_t b0 = lds32(kc), b1 = lds32(kc + 8);
-            mma_bf16_16816(st[j], dh, b0, b1);
-            mma_bf16_16816(st[j], dl, b0, b1);
+        for (int j = 0; j < NT; j += 2) {
+            uint32_t kb[4];
+            ldsm_x4_t(kb, cK + (lr8 + 8 * (lm & 1)) * KS + 8 * (j + (lm >> 1)));
+            mma_bf16_16816(st[j], dh, kb[0], kb[1]);
+            mma_bf16_16816(st[j], dl, kb[0], kb[1]);
+            mma_bf16_16816(st[j + 1], dh, kb[2], kb[3]);
+            mma_bf16_16816(st[j + 1], dl, kb[2], kb[3]);
         }
     }
 
