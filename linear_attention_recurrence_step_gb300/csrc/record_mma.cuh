@@ -51,6 +51,8 @@ namespace gdn {
 constexpr int kMmaChunk = 16;                 // timesteps per chunk (one k16 tile of MMA2)
 constexpr int kMmaWarps = 4;                  // warps per CTA
 constexpr int kMmaRows = 16 * kMmaWarps;      // state rows per CTA
+constexpr int kMmaCtasPerSm = 4;              // register budget: 128 per thread (no spills);
+                                              // measured faster than 3 (168) and than 8-warp CTAs
 constexpr int kWStride = 24;                  // bf16 stride of the rows of W and KQs^T (16 + pad)
 __host__ __device__ constexpr int mma_kstride(int dk) { return dk + 8; }  // padded bf16 k / q row
 
@@ -107,7 +109,7 @@ __device__ __forceinline__ uint32_t lds32(const __nv_bfloat16 *p) {
 }
 
 template <int DK>
-__global__ void __launch_bounds__(32 * kMmaWarps, 3) record_mma_kernel(const RecordArgs a) {
+__global__ void __launch_bounds__(32 * kMmaWarps, kMmaCtasPerSm) record_mma_kernel(const RecordArgs a) {
     using T = __nv_bfloat16;
     constexpr int NT = DK / 8;   // 8-column blocks of a state row
     constexpr int KT = DK / 16;  // k16 tiles along Dk
