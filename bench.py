@@ -194,10 +194,12 @@ def rank_seed(base_seed: int, rank: int) -> int:
     return base_seed + 7919 * rank
 
 
-def _make_rank_case(config: str, rank: int):
+def _make_rank_case(config: str, rank: int, batch=None):
     spec = dict(workloads.CONFIGS[config])
     seed = rank_seed(spec.pop("seed"), rank)
     spec.pop("repeat", None)
+    if batch is not None:
+        spec["B"] = int(batch)
     return workloads.make_case(seed=seed, name=config, **spec)
 
 
@@ -209,7 +211,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     lib = gdn.load()
-    case = _make_rank_case(args.config, rank)
+    case = _make_rank_case(args.config, rank, args.batch)
     uses_repeat = workloads.uses_repeat(args.config)
     dt = case.dtype
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dt]
@@ -452,7 +454,7 @@ def run_reference(args, rank, world):
         return None
     import oracle
     oracle.build()
-    case = workloads.make_config(args.config)
+    case = workloads.make_config(args.config, batch=args.batch)
     threads = oracle.max_threads()
     # size the per-step batch sample so the whole run stays within ~2 minutes
     one = _oracle_inputs(oracle, case, 1)
@@ -505,6 +507,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--batch", type=int, default=None,
+                   help="override B (smaller cases for profiler captures; not a bench line)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
