@@ -15,10 +15,13 @@ Parity status of each function (what pins it; tests/test_oracle_pins.py):
 * ``record`` -- pinned: hand-derived worked example (tests/golden), closed
   forms (outer-product write, reset g=0), the delta-rule projection identity
   at every step, an independent matrix-form restatement, permutation
-  equivariance, masked-step identity.
+  equivariance, masked-step identity; the tiled GQA mapping equals the
+  pinned repeat followed by a record on the expanded heads.
 * ``replay`` -- pinned: accepted=T reproduces record, accepted=a reproduces
   record on the first a tokens, accepted=0 / all-masked identity, NaN in
-  unused tape slots never reaches the state, worked example.
+  unused tape slots never reaches the state, worked example; per-sequence
+  accepted counts reproduce, sequence by sequence, a record over that
+  sequence's own prefix.
 * ``repeat_tiled`` -- pinned: numpy fancy indexing, bit-exact.
 """
 from __future__ import annotations
@@ -40,6 +43,7 @@ _default: Optional["OracleLib"] = None
 
 _D = ctypes.POINTER(ctypes.c_double)
 _U32 = ctypes.POINTER(ctypes.c_uint32)
+_P64 = ctypes.POINTER(ctypes.c_int64)
 _I64 = ctypes.c_int64
 
 
@@ -68,9 +72,9 @@ class OracleLib:
 
     def __init__(self, path: str):
         lib = ctypes.CDLL(path)
-        lib.gdn_oracle_record.argtypes = [_I64] * 6 + [_D] * 6 + [_U32] + [_D] * 5
+        lib.gdn_oracle_record.argtypes = [_I64] * 7 + [_D] * 6 + [_U32] + [_D] * 5
         lib.gdn_oracle_record.restype = None
-        lib.gdn_oracle_replay.argtypes = [_I64] * 6 + [_D] * 4 + [_U32, _D]
+        lib.gdn_oracle_replay.argtypes = [_I64] * 6 + [_P64] + [_D] * 4 + [_U32, _D]
         lib.gdn_oracle_replay.restype = None
         lib.gdn_oracle_repeat_tiled.argtypes = [_I64] * 5 + [ctypes.c_void_p] * 2
         lib.gdn_oracle_repeat_tiled.restype = None
@@ -140,13 +144,20 @@ def repeat_tiled(*a, **kw):
     return default().repeat_tiled(*a, **kw)
 
 
+GQA_MAPPINGS = {"block": 0, "tiled": 1}
+
+
 def _record(lib, q, k, v, g, beta, state, mask=None, *, capture_tape: bool = True,
-            fill: float = float("nan")):
+            fill: float = float("nan"), gqa: str = "block"):
     """Float64 record step.  Returns dict y, state_out, delta_log[, k_log, g_log].
 
     y / delta_log / k_log / g_log start filled with ``fill`` so that positions
-    the method leaves untouched (masked steps) stay recognisable.
+    the method leaves untouched (masked steps) stay recognisable.  ``gqa``
+    picks the key head of value head hv: "block" hv // (Hv/Hk), "tiled"
+    hv % Hk.
     """
+    if gqa not in GQA_MAPPINGS:
+        raise ValueError(f"gqa must be one of {sorted(GQA_MAPPINGS)}")
     q = np.asarray(q)
     B, T, Hk, Dk = q.shape
     Hv, Dv = np.asarray(v).shape[2], np.asarray(v).shape[3]
@@ -164,7 +175,7 @@ def _record(lib, q, k, v, g, beta, state, mask=None, *, capture_tape: bool = Tru
     s_out = np.empty((B, Hv, Dv, Dk))
     kl = np.full((B, T, Hv, Dk), fill) if capture_tape else None
     gl = np.full((B, T, Hv), fill) if capture_tape else None
-    lib.gdn_oracle_record(B, T, Hk, Hv, Dk, Dv, _dp(q), _dp(k), _dp(v), _dp(g),
+    lib.gdn_oracle_record(B, T, Hk, Hv, Dk, Dv, GQA_MAPPINGS[gqa], _dp(q), _dp(k), _dp(v), _dp(g),
                           _dp(beta), _dp(s_in), mp, _dp(y), _dp(s_out), _dp(dl),
                           _dp(kl), _dp(gl))
     out = dict(y=y, state_out=s_out, delta_log=dl)
@@ -173,20 +184,33 @@ def _record(lib, q, k, v, g, beta, state, mask=None, *, capture_tape: bool = Tru
     return out
 
 
-def _replay(lib, delta_log, k_log, g_log, state, mask=None, *, accepted: int):
-    """Float64 replay of the accepted tape prefix onto ``state``; returns state_out."""
+def _replay(lib, delta_log, k_log, g_log, state, mask=None, *, accepted):
+    """Float64 replay of the accepted tape prefix onto ``state``; returns state_out.
+
+    ``accepted`` is one int >= 0 for the whole batch, or a length-B sequence
+    of per-sequence counts (a negative entry accepts nothing).
+    """
     dl = np.asarray(delta_log)
     B, T, Hv, Dv = dl.shape
     Dk = np.asarray(k_log).shape[3]
-    if accepted < 0:
-        raise ValueError("accepted must be >= 0")
+    per_seq = None
+    if np.ndim(accepted) == 0:
+        if accepted < 0:
+            raise ValueError("accepted must be >= 0")
+        scalar = int(accepted)
+    else:
+        per_seq = np.ascontiguousarray(accepted, dtype=np.int64)
+        if per_seq.shape != (B,):
+            raise ValueError(f"per-sequence accepted must have shape ({B},)")
+        scalar = 0
     dl = _f64(dl, (B, T, Hv, Dv))
     kl = _f64(k_log, (B, T, Hv, Dk))
     gl = _f64(g_log, (B, T, Hv))
     s_in = _f64(state, (B, Hv, Dv, Dk))
     m, mp = _mask(mask, B, T)
     s_out = np.empty((B, Hv, Dv, Dk))
-    lib.gdn_oracle_replay(B, T, Hv, Dk, Dv, int(accepted), _dp(dl), _dp(kl), _dp(gl),
+    lib.gdn_oracle_replay(B, T, Hv, Dk, Dv, scalar,
+                          None if per_seq is None else per_seq.ctypes.data_as(_P64), _dp(dl), _dp(kl), _dp(gl),
                           _dp(s_in), mp, _dp(s_out))
     return s_out
 

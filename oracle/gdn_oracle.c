@@ -52,8 +52,12 @@ void gdn_oracle_set_threads(int n)
 /*
  * Record [P1, kernel gated_delta_step_record].
  *
- * For every row (b, hv, dv) with hk = hv / (Hv / Hk) (block GQA mapping) and
- * for t = 0 .. T-1 whose mask is on (mask == NULL means every step is on):
+ * For every row (b, hv, dv) and for t = 0 .. T-1 whose mask is on
+ * (mask == NULL means every step is on), with the key head
+ *     hk = hv / (Hv / Hk)   block GQA mapping (the record kernel's own rule),
+ *     hk = hv % Hk          tiled mapping when tiled_gqa != 0 ("mlx-native
+ *                           repeat_tiled.rs", module doc "Mapping": the head
+ *                           order of a tiled repeat, read in place):
  *     s      <- g[b,t,hv] * s
  *     kv      = sum_i s[i] * k[b,t,hk,i]
  *     delta   = (v[b,t,hv,dv] - kv) * beta[b,t,hv]
@@ -64,14 +68,15 @@ void gdn_oracle_set_threads(int n)
  * state_out[b,hv,dv,:] = s after the last step.
  *
  * Tape capture (module doc: k_log [B,T,Hv,Dk] "GQA-expanded", g_log
- * [B,T,Hv]): when k_log / g_log are non-NULL they receive k[b,t,hk,:] and
+ * [B,T,Hv]): when k_log / g_log are non-NULL they receive k[b,t,hk,:] (hk by
+ * the same mapping) and
  * g[b,t,hv] at exactly the (b,t,hv) positions where delta_log is written.
  *
  * Layouts (row-major): q,k [B,T,Hk,Dk]; v,y,delta_log [B,T,Hv,Dv];
  * g,beta,g_log [B,T,Hv]; k_log [B,T,Hv,Dk]; state [B,Hv,Dv,Dk]; mask [B,T].
  */
 void gdn_oracle_record(int64_t B, int64_t T, int64_t Hk, int64_t Hv,
-                       int64_t Dk, int64_t Dv,
+                       int64_t Dk, int64_t Dv, int64_t tiled_gqa,
                        const double *q, const double *k, const double *v,
                        const double *g, const double *beta,
                        const double *state_in, const uint32_t *mask,
@@ -84,7 +89,7 @@ void gdn_oracle_record(int64_t B, int64_t T, int64_t Hk, int64_t Hv,
     for (n = 0; n < B * Hv; ++n) {
         const int64_t b = n / Hv;
         const int64_t hv = n % Hv;
-        const int64_t hk = hv / group;
+        const int64_t hk = tiled_gqa ? hv % Hk : hv / group;
         double *s = (double *)malloc((size_t)Dk * sizeof(double));
         for (int64_t dv = 0; dv < Dv; ++dv) {
             const double *row_in = state_in + (n * Dv + dv) * Dk;
@@ -143,9 +148,14 @@ void gdn_oracle_record(int64_t B, int64_t T, int64_t Hk, int64_t Hv,
  * The selected-away branch is never evaluated here, so whatever a masked or
  * unaccepted tape slot holds (NaN included) cannot reach the state, as with
  * the page's select.  accepted >= T folds every step whose mask is on.
+ *
+ * Per-sequence acceptance (the module doc's speculative-decode use: each
+ * sequence of the batch keeps its own accepted prefix): when
+ * accepted_per_seq is non-NULL, sequence b uses accepted_per_seq[b] in place
+ * of the scalar; a negative entry accepts nothing.
  */
 void gdn_oracle_replay(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv,
-                       int64_t accepted,
+                       int64_t accepted, const int64_t *accepted_per_seq,
                        const double *delta_log, const double *k_log,
                        const double *g_log, const double *state_in,
                        const uint32_t *mask, double *state_out)
@@ -155,13 +165,14 @@ void gdn_oracle_replay(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv,
     for (n = 0; n < B * Hv; ++n) {
         const int64_t b = n / Hv;
         const int64_t hv = n % Hv;
+        const int64_t acc = accepted_per_seq ? accepted_per_seq[b] : accepted;
         double *s = (double *)malloc((size_t)Dk * sizeof(double));
         for (int64_t dv = 0; dv < Dv; ++dv) {
             const double *row_in = state_in + (n * Dv + dv) * Dk;
             for (int64_t i = 0; i < Dk; ++i) s[i] = row_in[i];
             for (int64_t t = 0; t < T; ++t) {
                 const uint32_t m = mask ? mask[b * T + t] : 1u;
-                const int do_step = (t < accepted) && (m != 0);
+                const int do_step = (t < acc) && (m != 0);
                 if (!do_step) continue;
                 const int64_t gi = (b * T + t) * Hv + hv;
                 const double gt = g_log[gi];

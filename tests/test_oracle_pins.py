@@ -14,7 +14,9 @@ is something the pages or the mathematics fix independently --
   S <- g S (I - beta k k^T) + beta v k^T, y = S q;
 * replay invariants (accepted = T, accepted = a, accepted = 0, all masked,
   NaN in unused tape slots);
-* equivariance under batch / value-row permutations, the block GQA mapping;
+* equivariance under batch / value-row permutations, the block GQA mapping,
+  and the tiled mapping as the pinned repeat followed by a record;
+* per-sequence accepted counts against a record over each sequence's prefix;
 * numpy fancy indexing for the repeat.
 
 ``test_pins_catch_planted_mistakes`` compiles mutated copies of the oracle
@@ -229,6 +231,46 @@ def check_gqa_block_mapping(orc):
         np.testing.assert_array_equal(out["y"][:, :, hv], one["y"][:, :, 0])
 
 
+def check_gqa_tiled_mapping(orc):
+    # the tiled mapping is the tiled repeat (pinned by numpy indexing in
+    # check_repeat) followed by a record on the expanded heads (Hk' = Hv)
+    c = _rand_case(62, B=2, T=4, Hk=2, Hv=6, Dk=5, Dv=3, mask="random")
+    out = orc.record(**c, gqa="tiled")
+    B, T, Hk, Dk = c["q"].shape
+    Hv = c["v"].shape[2]
+
+    def expand(x):
+        return orc.repeat_tiled(x.reshape(B * T, Hk, Dk), Hv).reshape(B, T, Hv, Dk)
+
+    ref = orc.record(expand(c["q"]), expand(c["k"]), c["v"], c["g"], c["beta"], c["state"],
+                     c["mask"])
+    for name in ("y", "delta_log", "state_out", "k_log", "g_log"):
+        np.testing.assert_array_equal(out[name], ref[name], err_msg=name)
+    # and it differs from the block mapping on the same inputs
+    blk = orc.record(**c)
+    assert not np.allclose(blk["state_out"], out["state_out"])
+
+
+def check_replay_per_sequence(orc):
+    # sequence b with its own accepted count a_b ends where a record over its
+    # first a_b tokens ends; negative counts accept nothing, counts past T
+    # accept everything
+    c = _rand_case(33, B=5, T=6, Hk=1, Hv=2, Dk=4, Dv=3, mask="random")
+    rec = orc.record(**c)
+    tape = (rec["delta_log"], rec["k_log"], rec["g_log"])
+    acc = np.array([0, 6, 3, -2, 9])
+    st = orc.replay(*tape, c["state"], c["mask"], accepted=acc)
+    for b in range(5):
+        a = int(min(max(acc[b], 0), 6))
+        if a == 0:
+            np.testing.assert_array_equal(st[b], c["state"][b])
+            continue
+        sub = {kk: (vv[b:b + 1] if kk == "state" else vv[b:b + 1, :a]) if vv is not None else None
+               for kk, vv in c.items()}
+        np.testing.assert_allclose(st[b], orc.record(**sub)["state_out"][0],
+                                   rtol=1e-12, atol=1e-12, err_msg=f"sequence {b}")
+
+
 def check_permutation_equivariance(orc):
     c = _rand_case(71, B=3, T=4, Hk=1, Hv=2, Dk=5, Dv=6, mask="random")
     out = orc.record(**c)
@@ -257,6 +299,7 @@ def check_repeat(orc):
 ALL_CHECKS = [check_worked_example, check_closed_form_outer_product, check_reset,
               check_projection_identity, check_matrix_form, check_replay_invariants,
               check_masked_steps, check_tape_capture, check_gqa_block_mapping,
+              check_gqa_tiled_mapping, check_replay_per_sequence,
               check_permutation_equivariance, check_repeat]
 
 
@@ -271,14 +314,17 @@ MUTANTS = {
     "delta_sign": ("const double delta = (v[vi] - kv) * bt;", "const double delta = (kv - v[vi]) * bt;"),
     "readout_before_update": ("s[i] = s[i] + kt[i] * delta;\n                    out += s[i] * qt[i];",
                               "out += s[i] * qt[i];\n                    s[i] = s[i] + kt[i] * delta;"),
-    "tiled_instead_of_block_gqa": ("const int64_t hk = hv / group;", "const int64_t hk = hv % Hk;"),
+    "tiled_instead_of_block_gqa": ("tiled_gqa ? hv % Hk : hv / group;", "hv % Hk;"),
+    "block_instead_of_tiled_gqa": ("tiled_gqa ? hv % Hk : hv / group;", "hv / group;"),
+    "per_seq_accepted_of_first_sequence": ("accepted_per_seq ? accepted_per_seq[b] : accepted;",
+                                           "accepted_per_seq ? accepted_per_seq[0] : accepted;"),
     "beta_dropped": ("const double delta = (v[vi] - kv) * bt;", "const double delta = (v[vi] - kv);"),
     "q_for_k_in_kv": ("kv += s[i] * kt[i];", "kv += s[i] * qt[i];"),
     "state_transposed": ("const double *row_in = state_in + (n * Dv + dv) * Dk;\n            for (int64_t i = 0; i < Dk; ++i) s[i] = row_in[i];\n            for (int64_t t = 0; t < T; ++t) {\n                const uint32_t m = mask ? mask[b * T + t] : 1u;\n                if (m == 0) continue;",
                          "const double *row_in = state_in + n * Dv * Dk;\n            for (int64_t i = 0; i < Dk; ++i) s[i] = row_in[i * Dv + dv];\n            for (int64_t t = 0; t < T; ++t) {\n                const uint32_t m = mask ? mask[b * T + t] : 1u;\n                if (m == 0) continue;"),
     "record_ignores_mask": ("                if (m == 0) continue;\n                const double *kt", "                (void)m;\n                const double *kt"),
-    "replay_ignores_accepted": ("const int do_step = (t < accepted) && (m != 0);", "const int do_step = (m != 0);"),
-    "replay_ignores_mask": ("const int do_step = (t < accepted) && (m != 0);", "const int do_step = (t < accepted);"),
+    "replay_ignores_accepted": ("const int do_step = (t < acc) && (m != 0);", "const int do_step = (m != 0);"),
+    "replay_ignores_mask": ("const int do_step = (t < acc) && (m != 0);", "const int do_step = (t < acc);"),
     "replay_additive_decay": ("s[i] = s[i] * gt + kt[i] * d;", "s[i] = s[i] + gt * kt[i] * d;"),
     "repeat_block_mapping": ("(t * hg + hh % hg) * kdim", "(t * hg + hh / (h / hg)) * kdim"),
 }
