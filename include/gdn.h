@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 1
+#define GDN_ABI_VERSION 2
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st *gdn_stream_t;
@@ -63,6 +63,14 @@ typedef enum gdn_dtype {
     GDN_DTYPE_BF16 = 1,
     GDN_DTYPE_F16 = 2
 } gdn_dtype;
+
+/* Which key head a value head reads (G = Hv / Hk). */
+typedef enum gdn_gqa_mapping {
+    GDN_GQA_BLOCK = 0, /* hk = hv / G: the record kernel's own rule             */
+    GDN_GQA_TILED = 1  /* hk = hv % Hk: the head order of the tiled repeat
+                          ("mlx-native repeat_tiled.rs", module doc "Mapping"),
+                          read in place instead of materialised             */
+} gdn_gqa_mapping;
 
 /*
  * gdn_step_record -- T recurrence steps with delta-tape capture
@@ -110,6 +118,27 @@ gdn_status gdn_step_record(const void *q, const void *k, const void *v,
                            gdn_stream_t stream);
 
 /*
+ * gdn_step_record_mapped -- gdn_step_record with a choice of GQA mapping.
+ *
+ * Identical to gdn_step_record (same arguments, layouts, errors) except that
+ * the key head of value head hv is chosen by `mapping`:
+ *   GDN_GQA_BLOCK  hk = hv / (Hv/Hk)  (gdn_step_record itself)
+ *   GDN_GQA_TILED  hk = hv % Hk       (the result equals gqa_repeat_tiled of
+ *                  q and k to Hv heads followed by gdn_step_record with
+ *                  Hk = Hv, without the expanded copies)
+ * k_log, when given, receives k[b,t,hk,:] under the same mapping.  An
+ * unknown mapping value is GDN_ERR_INVALID_ARGUMENT.
+ */
+gdn_status gdn_step_record_mapped(const void *q, const void *k, const void *v,
+                                  const void *g, const void *beta,
+                                  const float *state_in, const uint32_t *mask,
+                                  void *y, float *state_out, void *delta_log,
+                                  void *k_log, void *g_log,
+                                  int64_t B, int64_t T, int64_t Hk, int64_t Hv,
+                                  int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
+                                  gdn_dtype dtype, gdn_stream_t stream);
+
+/*
  * gdn_state_replay -- rebuild the state after an accepted prefix of the tape
  * (page: state_replay; module doc: "re-folds the accepted prefix").
  *
@@ -137,6 +166,27 @@ gdn_status gdn_state_replay(const void *delta_log, const void *k_log,
                             int64_t B, int64_t T, int64_t Hv, int64_t Dk,
                             int64_t Dv, int64_t accepted, gdn_dtype dtype,
                             gdn_stream_t stream);
+
+/*
+ * gdn_state_replay_per_seq -- gdn_state_replay with one accepted count per
+ * sequence (speculative decoding accepts a different draft prefix in every
+ * sequence of the batch; the page's kernel takes one count per dispatch).
+ *
+ *   accepted   [B] int32, DEVICE memory, 4-byte aligned, non-NULL.  Sequence
+ *              b folds the steps t < accepted[b] whose mask is on; an entry
+ *              < 0 acts as 0 (the sequence's state_out is its snapshot) and
+ *              an entry > T acts as T.  Read by the kernel, so it may be
+ *              produced by earlier work on the same stream.
+ * Every other argument, layout and error is as for gdn_state_replay.  With
+ * the same tape, sequence b's result equals gdn_state_replay with
+ * accepted = accepted[b] (bit for bit).
+ */
+gdn_status gdn_state_replay_per_seq(const void *delta_log, const void *k_log,
+                                    const void *g_log, const float *state_in,
+                                    const uint32_t *mask, float *state_out,
+                                    int64_t B, int64_t T, int64_t Hv, int64_t Dk,
+                                    int64_t Dv, const int32_t *accepted,
+                                    gdn_dtype dtype, gdn_stream_t stream);
 
 /*
  * gqa_repeat_tiled -- tiled GQA broadcast (page: repeat_tiled.rs, "Mapping"):

@@ -12,8 +12,12 @@ Entry points (same names as the C ABI):
 * ``gdn_step_record`` -- T gated delta-rule steps; writes y, the final state
   and the delta tape (optionally k_log / g_log), "metaltile-std
   gated_delta_replay.rs", kernel gated_delta_step_record.
+* ``gdn_step_record_mapped`` -- the same with the tiled GQA mapping
+  ``hk = hv % Hk`` available (``mapping="tiled"``).
 * ``gdn_state_replay`` -- re-fold the accepted tape prefix onto a snapshot,
   same page, kernel state_replay.
+* ``gdn_state_replay_per_seq`` -- the same with one accepted count per
+  sequence (an int32 device tensor).
 * ``gqa_repeat_tiled`` -- ``dst[t,h,k] = src[t,h%hg,k]``, "mlx-native
   repeat_tiled.rs".
 """
@@ -29,13 +33,16 @@ import torch
 
 from . import _build
 
-__all__ = ["GdnError", "build", "load", "lib_path", "gdn_step_record", "gdn_state_replay",
-           "gqa_repeat_tiled", "RecordOutputs", "STATUS_NAMES", "DTYPE_CODES"]
+__all__ = ["GdnError", "build", "load", "lib_path", "gdn_step_record", "gdn_step_record_mapped",
+           "gdn_state_replay", "gdn_state_replay_per_seq", "gqa_repeat_tiled", "RecordOutputs",
+           "STATUS_NAMES", "DTYPE_CODES", "GQA_MAPPINGS"]
 
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPORTED",
                 3: "GDN_ERR_MISALIGNED", 4: "GDN_ERR_CUDA"}
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
-EXPORTED = ("gdn_step_record", "gdn_state_replay", "gqa_repeat_tiled", "gdn_status_string",
+GQA_MAPPINGS = {"block": 0, "tiled": 1}
+EXPORTED = ("gdn_step_record", "gdn_step_record_mapped", "gdn_state_replay",
+            "gdn_state_replay_per_seq", "gqa_repeat_tiled", "gdn_status_string",
             "gdn_last_error", "gdn_abi_version")
 
 RecordOutputs = namedtuple("RecordOutputs", "y state_out delta_log k_log g_log")
@@ -66,8 +73,12 @@ def build(force: bool = False) -> str:
 def _declare(lib: ctypes.CDLL) -> None:
     lib.gdn_step_record.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int, _P]
     lib.gdn_step_record.restype = ctypes.c_int
+    lib.gdn_step_record_mapped.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int] * 2 + [_P]
+    lib.gdn_step_record_mapped.restype = ctypes.c_int
     lib.gdn_state_replay.argtypes = [_P] * 6 + [_I] * 6 + [ctypes.c_int, _P]
     lib.gdn_state_replay.restype = ctypes.c_int
+    lib.gdn_state_replay_per_seq.argtypes = [_P] * 6 + [_I] * 5 + [_P, ctypes.c_int, _P]
+    lib.gdn_state_replay_per_seq.restype = ctypes.c_int
     lib.gqa_repeat_tiled.argtypes = [_P, _P] + [_I] * 4 + [ctypes.c_int, ctypes.c_size_t,
                                                             ctypes.c_size_t, _P]
     lib.gqa_repeat_tiled.restype = ctypes.c_int
@@ -128,10 +139,14 @@ def _need(t: torch.Tensor, name: str, shape, dtype, device) -> None:
 
 def gdn_step_record(q, k, v, g, beta, state_in, mask=None, *, y=None, state_out=None,
                     delta_log=None, k_log=None, g_log=None, capture_tape: bool = False,
-                    stream=None) -> RecordOutputs:
+                    gqa: str = "block", stream=None) -> RecordOutputs:
     """Run T record steps.  Missing outputs are allocated (uninitialised where
     the mask skips a step).  ``capture_tape=True`` also allocates k_log/g_log.
-    ``state_out=state_in`` runs in place."""
+    ``state_out=state_in`` runs in place.  ``gqa="tiled"`` reads key head
+    ``hv % Hk`` (C entry point gdn_step_record_mapped) instead of the block
+    mapping ``hv // (Hv/Hk)``."""
+    if gqa not in GQA_MAPPINGS:
+        raise ValueError(f"gqa must be one of {sorted(GQA_MAPPINGS)}")
     B, T, Hk, Dk = q.shape
     Hv, Dv = v.shape[2], v.shape[3]
     dt, dev = q.dtype, q.device
@@ -163,17 +178,31 @@ def gdn_step_record(q, k, v, g, beta, state_in, mask=None, *, y=None, state_out=
         _need(k_log, "k_log", (B, T, Hv, Dk), dt, dev)
     if g_log is not None:
         _need(g_log, "g_log", (B, T, Hv), dt, dev)
-    st = load().gdn_step_record(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(mask), _ptr(y),
-        _ptr(state_out), _ptr(delta_log), _ptr(k_log), _ptr(g_log), B, T, Hk, Hv, Dk, Dv,
-        DTYPE_CODES[dt], _stream(dev, stream))
-    _check(st, "gdn_step_record")
+    ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(mask), _ptr(y),
+            _ptr(state_out), _ptr(delta_log), _ptr(k_log), _ptr(g_log), B, T, Hk, Hv, Dk, Dv)
+    if gqa == "block":
+        st = load().gdn_step_record(*ptrs, DTYPE_CODES[dt], _stream(dev, stream))
+        _check(st, "gdn_step_record")
+    else:
+        st = load().gdn_step_record_mapped(*ptrs, GQA_MAPPINGS[gqa], DTYPE_CODES[dt],
+                                           _stream(dev, stream))
+        _check(st, "gdn_step_record_mapped")
     return RecordOutputs(y, state_out, delta_log, k_log, g_log)
 
 
-def gdn_state_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted: int,
+def gdn_step_record_mapped(q, k, v, g, beta, state_in, mask=None, *, mapping: str,
+                           **kw) -> RecordOutputs:
+    """``gdn_step_record`` with an explicit GQA mapping ("block" or "tiled")."""
+    return gdn_step_record(q, k, v, g, beta, state_in, mask, gqa=mapping, **kw)
+
+
+def gdn_state_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted,
                      state_out=None, stream=None) -> torch.Tensor:
-    """Fold the tape prefix [0, accepted) onto ``state_in``; returns state_out."""
+    """Fold the tape prefix [0, accepted) onto ``state_in``; returns state_out.
+
+    ``accepted`` is an int (one count for the batch) or an int32 device
+    tensor of shape [B] (one count per sequence; C entry point
+    gdn_state_replay_per_seq)."""
     B, T, Hv, Dv = delta_log.shape
     Dk = k_log.shape[3]
     dt, dev = delta_log.dtype, delta_log.device
@@ -188,11 +217,25 @@ def gdn_state_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted: 
     if state_out is None:
         state_out = torch.empty_like(state_in)
     _need(state_out, "state_out", (B, Hv, Dv, Dk), torch.float32, dev)
-    st = load().gdn_state_replay(
-        _ptr(delta_log), _ptr(k_log), _ptr(g_log), _ptr(state_in), _ptr(mask), _ptr(state_out),
-        B, T, Hv, Dk, Dv, int(accepted), DTYPE_CODES[dt], _stream(dev, stream))
-    _check(st, "gdn_state_replay")
+    ptrs = (_ptr(delta_log), _ptr(k_log), _ptr(g_log), _ptr(state_in), _ptr(mask),
+            _ptr(state_out), B, T, Hv, Dk, Dv)
+    if isinstance(accepted, torch.Tensor):
+        _need(accepted, "accepted", (B,), torch.int32, dev)
+        st = load().gdn_state_replay_per_seq(*ptrs, _ptr(accepted), DTYPE_CODES[dt],
+                                             _stream(dev, stream))
+        _check(st, "gdn_state_replay_per_seq")
+    else:
+        st = load().gdn_state_replay(*ptrs, int(accepted), DTYPE_CODES[dt], _stream(dev, stream))
+        _check(st, "gdn_state_replay")
     return state_out
+
+
+def gdn_state_replay_per_seq(delta_log, k_log, g_log, state_in, mask=None, *,
+                             accepted: torch.Tensor, **kw) -> torch.Tensor:
+    """``gdn_state_replay`` with per-sequence accepted counts ([B] int32, device)."""
+    if not isinstance(accepted, torch.Tensor):
+        raise TypeError("accepted must be an int32 device tensor of shape [B]")
+    return gdn_state_replay(delta_log, k_log, g_log, state_in, mask, accepted=accepted, **kw)
 
 
 def gqa_repeat_tiled(src, h: int, *, dst=None, stream=None) -> torch.Tensor:

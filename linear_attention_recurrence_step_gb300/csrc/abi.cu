@@ -59,8 +59,8 @@ int elem_bytes(gdn_dtype dt) {
     return 0;
 }
 
-gdn_status cuda_fail(const char *what, cudaError_t e) {
-    return fail(GDN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+gdn_status cuda_fail(const char *fn, const char *what, cudaError_t e) {
+    return fail(GDN_ERR_CUDA, "%s: %s: %s (%s)", fn, what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
 // SM count of the current device (0 if it cannot be read).
@@ -174,109 +174,159 @@ const char *gdn_last_error(void) { return g_last_error.c_str(); }
 
 int gdn_abi_version(void) { return GDN_ABI_VERSION; }
 
-gdn_status gdn_step_record(const void *q, const void *k, const void *v, const void *g,
-                           const void *beta, const float *state_in, const uint32_t *mask,
-                           void *y, float *state_out, void *delta_log, void *k_log, void *g_log,
-                           int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
-                           gdn_dtype dtype, gdn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+gdn_status record_impl(const char *fn, const void *q, const void *k, const void *v, const void *g,
+                       const void *beta, const float *state_in, const uint32_t *mask, void *y,
+                       float *state_out, void *delta_log, void *k_log, void *g_log, int64_t B,
+                       int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                       gdn_gqa_mapping mapping, gdn_dtype dtype, gdn_stream_t stream) {
     const int eb = elem_bytes(dtype);
-    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "gdn_step_record: unknown dtype %d", (int)dtype);
+    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dtype);
+    if (mapping != GDN_GQA_BLOCK && mapping != GDN_GQA_TILED)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: unknown GQA mapping %d", fn, (int)mapping);
     if (B <= 0 || T <= 0 || Hk <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0)
         return fail(GDN_ERR_INVALID_ARGUMENT,
-                    "gdn_step_record: B, T, Hk, Hv, Dk, Dv must all be > 0 (got %lld %lld %lld %lld %lld %lld)",
+                    "%s: B, T, Hk, Hv, Dk, Dv must all be > 0 (got %lld %lld %lld %lld %lld %lld)", fn,
                     (long long)B, (long long)T, (long long)Hk, (long long)Hv, (long long)Dk, (long long)Dv);
     if (Hv % Hk != 0)
-        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: Hv (%lld) must be a multiple of Hk (%lld)",
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: Hv (%lld) must be a multiple of Hk (%lld)", fn,
                     (long long)Hv, (long long)Hk);
     if (!q || !k || !v || !g || !beta || !state_in || !y || !state_out || !delta_log)
         return fail(GDN_ERR_INVALID_ARGUMENT,
-                    "gdn_step_record: q, k, v, g, beta, state_in, y, state_out, delta_log must be non-NULL");
+                    "%s: q, k, v, g, beta, state_in, y, state_out, delta_log must be non-NULL", fn);
     if (Dk % 32 != 0 || !gdn::supported_dk(Dk))
-        return fail(GDN_ERR_UNSUPPORTED, "gdn_step_record: Dk = %lld not supported (32, 64, 128, 192, 256)",
+        return fail(GDN_ERR_UNSUPPORTED, "%s: Dk = %lld not supported (32, 64, 128, 192, 256)", fn,
                     (long long)Dk);
     const int64_t qk_b = nbytes({B, T, Hk, Dk}, eb), v_b = nbytes({B, T, Hv, Dv}, eb);
     const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), kl_b = nbytes({B, T, Hv, Dk}, eb);
     const int64_t gb_b = nbytes({B, T, Hv}, eb), m_b = nbytes({B, T}, 4);
     if (qk_b < 0 || v_b < 0 || s_b < 0 || kl_b < 0 || gb_b < 0 || m_b < 0)
-        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: tensor sizes overflow int64");
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: tensor sizes overflow int64", fn);
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(state_in, 16) || !aligned(state_out, 16) ||
         !aligned(k_log, 16))
-        return fail(GDN_ERR_MISALIGNED,
-                    "gdn_step_record: q, k, state_in, state_out, k_log must be 16-byte aligned");
+        return fail(GDN_ERR_MISALIGNED, "%s: q, k, state_in, state_out, k_log must be 16-byte aligned",
+                    fn);
     if (!aligned(v, eb) || !aligned(g, eb) || !aligned(beta, eb) || !aligned(y, eb) ||
         !aligned(delta_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4))
-        return fail(GDN_ERR_MISALIGNED, "gdn_step_record: a tensor is not aligned to its element size");
+        return fail(GDN_ERR_MISALIGNED, "%s: a tensor is not aligned to its element size", fn);
     if (state_in != state_out && overlap(state_in, s_b, state_out, s_b))
         return fail(GDN_ERR_INVALID_ARGUMENT,
-                    "gdn_step_record: state_out overlaps state_in without being the same buffer");
+                    "%s: state_out overlaps state_in without being the same buffer", fn);
 
     cudaError_t e;
     const int sms = current_sm_count(&e);
-    if (e != cudaSuccess) return cuda_fail("gdn_step_record: device query", e);
+    if (e != cudaSuccess) return cuda_fail(fn, "device query", e);
     const gdn::Geometry geo =
         gdn::record_geometry((int)Dk, B * Hv, Dv, T, eb, dtype == GDN_DTYPE_BF16, sms);
     if ((B * Hv) > (int64_t)INT32_MAX / geo.row_blocks)
-        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_step_record: grid too large (B*Hv*row_blocks > 2^31-1)");
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large (B*Hv*row_blocks > 2^31-1)", fn);
     gdn::RecordArgs a{q, k, v, g, beta, state_in, mask, y, state_out, delta_log, k_log, g_log,
                       B, T, Hk, Hv, Dv, geo.rows_cta, geo.row_blocks, geo.tc,
-                      aligned(v, 16) && (Dv * eb) % 16 == 0};
+                      aligned(v, 16) && (Dv * eb) % 16 == 0, mapping == GDN_GQA_TILED};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (dtype) {
     case GDN_DTYPE_F32: e = gdn::launch_record_f32((int)Dk, a, geo, s); break;
     case GDN_DTYPE_BF16: e = gdn::launch_record_bf16((int)Dk, a, geo, s); break;
     case GDN_DTYPE_F16: e = gdn::launch_record_f16((int)Dk, a, geo, s); break;
     }
-    if (e != cudaSuccess) return cuda_fail("gdn_step_record: launch", e);
+    if (e != cudaSuccess) return cuda_fail(fn, "launch", e);
     return ok();
+}
+
+gdn_status replay_impl(const char *fn, const void *delta_log, const void *k_log, const void *g_log,
+                       const float *state_in, const uint32_t *mask, float *state_out, int64_t B,
+                       int64_t T, int64_t Hv, int64_t Dk, int64_t Dv, int64_t accepted,
+                       const int32_t *accepted_per_seq, gdn_dtype dtype, gdn_stream_t stream) {
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dtype);
+    if (B <= 0 || T <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: B, T, Hv, Dk, Dv must all be > 0 (got %lld %lld %lld %lld %lld)", fn,
+                    (long long)B, (long long)T, (long long)Hv, (long long)Dk, (long long)Dv);
+    if (accepted < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: accepted (%lld) must be >= 0", fn,
+                    (long long)accepted);
+    if (!delta_log || !k_log || !g_log || !state_in || !state_out)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: delta_log, k_log, g_log, state_in, state_out must be non-NULL", fn);
+    if (Dk % 32 != 0 || !gdn::supported_dk(Dk))
+        return fail(GDN_ERR_UNSUPPORTED, "%s: Dk = %lld not supported (32, 64, 128, 192, 256)", fn,
+                    (long long)Dk);
+    const int64_t d_b = nbytes({B, T, Hv, Dv}, eb), kl_b = nbytes({B, T, Hv, Dk}, eb);
+    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), g_b = nbytes({B, T, Hv}, eb);
+    const int64_t m_b = nbytes({B, T}, 4);
+    if (d_b < 0 || kl_b < 0 || s_b < 0 || g_b < 0 || m_b < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: tensor sizes overflow int64", fn);
+    if (!aligned(k_log, 16) || !aligned(state_in, 16) || !aligned(state_out, 16))
+        return fail(GDN_ERR_MISALIGNED, "%s: k_log, state_in, state_out must be 16-byte aligned", fn);
+    if (!aligned(delta_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4) ||
+        !aligned(accepted_per_seq, 4))
+        return fail(GDN_ERR_MISALIGNED, "%s: a tensor is not aligned to its element size", fn);
+    if (state_in != state_out && overlap(state_in, s_b, state_out, s_b))
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: state_out overlaps state_in without being the same buffer", fn);
+
+    const int64_t steps = accepted < T ? accepted : T;
+    if (!accepted_per_seq && steps == 0 && state_in == state_out)
+        return ok();  // identity, nothing to do
+    cudaError_t e;
+    const int sms = current_sm_count(&e);
+    if (e != cudaSuccess) return cuda_fail(fn, "device query", e);
+    const gdn::Geometry geo = gdn::replay_geometry((int)Dk, B * Hv, Dv, steps, eb, sms);
+    if ((B * Hv) > (int64_t)INT32_MAX / geo.row_blocks)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large", fn);
+    gdn::ReplayArgs a{delta_log, k_log, g_log, state_in, mask, state_out, B, T, Hv, Dv, steps,
+                      geo.rows_cta, geo.row_blocks, geo.tc,
+                      aligned(delta_log, 16) && (Dv * eb) % 16 == 0, accepted_per_seq};
+    e = gdn::launch_replay(static_cast<gdn::DType>(dtype), (int)Dk, a, geo,
+                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(fn, "launch", e);
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_step_record(const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, const float *state_in, const uint32_t *mask,
+                           void *y, float *state_out, void *delta_log, void *k_log, void *g_log,
+                           int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                           gdn_dtype dtype, gdn_stream_t stream) {
+    return record_impl("gdn_step_record", q, k, v, g, beta, state_in, mask, y, state_out,
+                       delta_log, k_log, g_log, B, T, Hk, Hv, Dk, Dv, GDN_GQA_BLOCK, dtype, stream);
+}
+
+gdn_status gdn_step_record_mapped(const void *q, const void *k, const void *v, const void *g,
+                                  const void *beta, const float *state_in, const uint32_t *mask,
+                                  void *y, float *state_out, void *delta_log, void *k_log,
+                                  void *g_log, int64_t B, int64_t T, int64_t Hk, int64_t Hv,
+                                  int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
+                                  gdn_dtype dtype, gdn_stream_t stream) {
+    return record_impl("gdn_step_record_mapped", q, k, v, g, beta, state_in, mask, y, state_out,
+                       delta_log, k_log, g_log, B, T, Hk, Hv, Dk, Dv, mapping, dtype, stream);
 }
 
 gdn_status gdn_state_replay(const void *delta_log, const void *k_log, const void *g_log,
                             const float *state_in, const uint32_t *mask, float *state_out,
                             int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv,
                             int64_t accepted, gdn_dtype dtype, gdn_stream_t stream) {
-    const int eb = elem_bytes(dtype);
-    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "gdn_state_replay: unknown dtype %d", (int)dtype);
-    if (B <= 0 || T <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0)
-        return fail(GDN_ERR_INVALID_ARGUMENT,
-                    "gdn_state_replay: B, T, Hv, Dk, Dv must all be > 0 (got %lld %lld %lld %lld %lld)",
-                    (long long)B, (long long)T, (long long)Hv, (long long)Dk, (long long)Dv);
-    if (accepted < 0)
-        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay: accepted (%lld) must be >= 0",
-                    (long long)accepted);
-    if (!delta_log || !k_log || !g_log || !state_in || !state_out)
-        return fail(GDN_ERR_INVALID_ARGUMENT,
-                    "gdn_state_replay: delta_log, k_log, g_log, state_in, state_out must be non-NULL");
-    if (Dk % 32 != 0 || !gdn::supported_dk(Dk))
-        return fail(GDN_ERR_UNSUPPORTED, "gdn_state_replay: Dk = %lld not supported (32, 64, 128, 192, 256)",
-                    (long long)Dk);
-    const int64_t d_b = nbytes({B, T, Hv, Dv}, eb), kl_b = nbytes({B, T, Hv, Dk}, eb);
-    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), g_b = nbytes({B, T, Hv}, eb);
-    const int64_t m_b = nbytes({B, T}, 4);
-    if (d_b < 0 || kl_b < 0 || s_b < 0 || g_b < 0 || m_b < 0)
-        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay: tensor sizes overflow int64");
-    if (!aligned(k_log, 16) || !aligned(state_in, 16) || !aligned(state_out, 16))
-        return fail(GDN_ERR_MISALIGNED, "gdn_state_replay: k_log, state_in, state_out must be 16-byte aligned");
-    if (!aligned(delta_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4))
-        return fail(GDN_ERR_MISALIGNED, "gdn_state_replay: a tensor is not aligned to its element size");
-    if (state_in != state_out && overlap(state_in, s_b, state_out, s_b))
-        return fail(GDN_ERR_INVALID_ARGUMENT,
-                    "gdn_state_replay: state_out overlaps state_in without being the same buffer");
+    return replay_impl("gdn_state_replay", delta_log, k_log, g_log, state_in, mask, state_out, B,
+                       T, Hv, Dk, Dv, accepted, nullptr, dtype, stream);
+}
 
-    const int64_t steps = accepted < T ? accepted : T;
-    if (steps == 0 && state_in == state_out) return ok();  // identity, nothing to do
-    cudaError_t e;
-    const int sms = current_sm_count(&e);
-    if (e != cudaSuccess) return cuda_fail("gdn_state_replay: device query", e);
-    const gdn::Geometry geo = gdn::replay_geometry((int)Dk, B * Hv, Dv, steps, eb, sms);
-    if ((B * Hv) > (int64_t)INT32_MAX / geo.row_blocks)
-        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay: grid too large");
-    gdn::ReplayArgs a{delta_log, k_log, g_log, state_in, mask, state_out, B, T, Hv, Dv, steps,
-                      geo.rows_cta, geo.row_blocks, geo.tc,
-                      aligned(delta_log, 16) && (Dv * eb) % 16 == 0};
-    e = gdn::launch_replay(static_cast<gdn::DType>(dtype), (int)Dk, a, geo,
-                           reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail("gdn_state_replay: launch", e);
-    return ok();
+gdn_status gdn_state_replay_per_seq(const void *delta_log, const void *k_log, const void *g_log,
+                                    const float *state_in, const uint32_t *mask,
+                                    float *state_out, int64_t B, int64_t T, int64_t Hv,
+                                    int64_t Dk, int64_t Dv, const int32_t *accepted,
+                                    gdn_dtype dtype, gdn_stream_t stream) {
+    if (!accepted)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay_per_seq: accepted must be non-NULL");
+    return replay_impl("gdn_state_replay_per_seq", delta_log, k_log, g_log, state_in, mask,
+                       state_out, B, T, Hv, Dk, Dv, T, accepted, dtype, stream);
 }
 
 gdn_status gqa_repeat_tiled(const void *src, void *dst, int64_t seq, int64_t hg, int64_t h,
@@ -307,7 +357,7 @@ gdn_status gqa_repeat_tiled(const void *src, void *dst, int64_t seq, int64_t hg,
 
     cudaError_t e;
     const int sms = current_sm_count(&e);
-    if (e != cudaSuccess) return cuda_fail("gqa_repeat_tiled: device query", e);
+    if (e != cudaSuccess) return cuda_fail("gqa_repeat_tiled", "device query", e);
     gdn::RepeatArgs a;
     a.src = src;
     a.dst = dst;
@@ -318,7 +368,7 @@ gdn_status gqa_repeat_tiled(const void *src, void *dst, int64_t seq, int64_t hg,
     a.elem_bytes = eb;
     a.vec16 = (a.row_bytes % 16 == 0) && aligned(src, 16) && aligned(dst, 16);
     e = gdn::launch_repeat(a, reinterpret_cast<cudaStream_t>(stream), sms);
-    if (e != cudaSuccess) return cuda_fail("gqa_repeat_tiled: launch", e);
+    if (e != cudaSuccess) return cuda_fail("gqa_repeat_tiled", "launch", e);
     return ok();
 }
 

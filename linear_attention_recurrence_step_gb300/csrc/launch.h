@@ -33,6 +33,7 @@ struct RecordArgs {
     int64_t row_blocks;
     int tc;
     bool vec_v;     // v rows can be copied in 16-byte pieces (aligned base, Dv*size % 16 == 0)
+    bool tiled_gqa; // key head of value head hv: hv % Hk (tiled) instead of hv / (Hv/Hk) (block)
 };
 
 struct ReplayArgs {
@@ -46,6 +47,9 @@ struct ReplayArgs {
     int64_t row_blocks;
     int tc;
     bool vec_d;     // delta_log rows can be copied in 16-byte pieces
+    const int32_t *acc_b;  // per-sequence accepted counts [B] (device) or null: then
+                           // steps applies to every sequence; else sequence b folds
+                           // min(max(acc_b[b], 0), steps) steps
 };
 
 struct RepeatArgs {

@@ -56,7 +56,7 @@ record_kernel(const RecordArgs a) {
     const int64_t n = blockIdx.x / a.row_blocks;
     const int64_t rb = blockIdx.x - n * a.row_blocks;
     const int64_t b = n / a.Hv, hv = n - b * a.Hv;
-    const int64_t hk = hv / (a.Hv / a.Hk);
+    const int64_t hk = a.tiled_gqa ? hv % a.Hk : hv / (a.Hv / a.Hk);  // key head of hv
     const int64_t row0 = rb * R;
     const int vlim = (int)min((int64_t)R, a.Dv - row0);  // live rows of this block
     const int lr0 = warp * RW + gi * RT;                 // this thread's first local row

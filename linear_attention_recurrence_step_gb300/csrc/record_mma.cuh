@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(32 * kMmaWarps, kMmaCtasPerSm) record_mma_kern
     const int64_t n = blockIdx.x / a.row_blocks;
     const int64_t rb = blockIdx.x - n * a.row_blocks;
     const int64_t b = n / a.Hv, hv = n - b * a.Hv;
-    const int64_t hk = hv / (a.Hv / a.Hk);
+    const int64_t hk = a.tiled_gqa ? hv % a.Hk : hv / (a.Hv / a.Hk);  // key head of hv
     const int64_t row0 = rb * R;
     const int vlim = (int)min((int64_t)R, a.Dv - row0);
     const int lr[2] = {warp * 16 + g, warp * 16 + g + 8};  // this lane's two local rows

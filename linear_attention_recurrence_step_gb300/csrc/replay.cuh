@@ -5,7 +5,9 @@
 //     s <- select(do_step, s g_t + k_t delta_t, s)
 // The page evaluates both arms for every t < T and selects; here the step
 // flag is uniform per CTA, so skipped steps are branched over and their tape
-// slots (and every slot at t >= accepted) are never read.
+// slots (and every slot at t >= accepted) are never read.  With per-sequence
+// accepted counts (one per b) the count is read once per CTA, since a CTA's
+// rows all belong to one sequence.
 //
 // The fold uses the same scaled state s = G s^ and the same f32 operations as
 // the record kernel (G' = G g, fold the scale when G' leaves range, else
@@ -73,10 +75,17 @@ replay_kernel(const ReplayArgs a) {
     const TIn *klp = static_cast<const TIn *>(a.k_log);
     const TIn *glp = static_cast<const TIn *>(a.g_log);
 
+    // steps this CTA folds: uniform per CTA (one sequence b per CTA)
+    int64_t steps = a.steps;
+    if (a.acc_b) {
+        const int64_t ab = (int64_t)__ldg(a.acc_b + b);
+        steps = ab < 0 ? 0 : (ab < steps ? ab : steps);
+    }
+
     float pre_g = 1.f;
     auto issue = [&](int64_t c) -> unsigned {
         const int64_t t0 = c * TC;
-        const int tcnt = (int)min((int64_t)TC, a.steps - t0);
+        const int tcnt = (int)min((int64_t)TC, steps - t0);
         const int slot = (int)(c & 1);
         const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
         const int64_t row_first = (b * a.T + t0) * a.Hv + hv;  // (b, t0, hv)
@@ -97,13 +106,13 @@ replay_kernel(const ReplayArgs a) {
     };
 
     Slice<Lay> s;
-    const int64_t nchunks = (a.steps + TC - 1) / TC;
+    const int64_t nchunks = (steps + TC - 1) / TC;
     unsigned next_bits = nchunks > 0 ? issue(0) : 0u;
     load_rows<Lay>(s, a.state_in, n, a.Dv, row0 + lr0, j);
     float G_sched = 1.f;
 
     for (int64_t c = 0; c < nchunks; ++c) {
-        const int tcnt = (int)min((int64_t)TC, a.steps - c * TC);
+        const int tcnt = (int)min((int64_t)TC, steps - c * TC);
         const int slot = (int)(c & 1);
         const unsigned bits = next_bits;
         cp_async_wait_all();

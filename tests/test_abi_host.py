@@ -44,15 +44,17 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for want in ("gdn_step_record", "gdn_state_replay", "gqa_repeat_tiled",
+    for want in ("gdn_step_record", "gdn_step_record_mapped", "gdn_state_replay",
+                 "gdn_state_replay_per_seq", "gqa_repeat_tiled",
                  "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
         assert want in names
+    assert set(names) == set(gdn.EXPORTED)
 
 
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libgdn.so does not export {name}"
-    assert lib.gdn_abi_version() == 1
+    assert lib.gdn_abi_version() == 2
 
 
 def test_library_is_sm103a():
@@ -81,6 +83,22 @@ def rep(lib, **kw):
                 stream=None)
     args.update(kw)
     return lib.gdn_state_replay(*args.values())
+
+
+def rec_mapped(lib, mapping=1, **kw):
+    args = dict(q=P(0), k=P(1), v=P(2), g=P(3), beta=P(4), state_in=P(5), mask=None,
+                y=P(6), state_out=P(7), delta_log=P(8), k_log=None, g_log=None,
+                B=2, T=3, Hk=2, Hv=4, Dk=64, Dv=32, mapping=mapping, dtype=BF16, stream=None)
+    args.update(kw)
+    return lib.gdn_step_record_mapped(*args.values())
+
+
+def rep_seq(lib, **kw):
+    args = dict(delta_log=P(0), k_log=P(1), g_log=P(2), state_in=P(3), mask=None,
+                state_out=P(4), B=2, T=3, Hv=4, Dk=64, Dv=32, accepted=P(5), dtype=BF16,
+                stream=None)
+    args.update(kw)
+    return lib.gdn_state_replay_per_seq(*args.values())
 
 
 def rpt(lib, **kw):
@@ -118,6 +136,41 @@ def test_record_rejects(lib, name):
     kw, want = RECORD_CASES[name]
     assert rec(lib, **kw) == want
     assert lib.gdn_last_error().decode().startswith("gdn_step_record")
+
+
+MAPPED_CASES = {
+    "mapping=2": (dict(mapping=2), INVALID),
+    "mapping=-1": (dict(mapping=-1), INVALID),
+    "tiled Hv%Hk": (dict(Hk=3), INVALID),
+    "tiled B=0": (dict(B=0), INVALID),
+    "tiled Dk=96": (dict(Dk=96), UNSUPPORTED),
+    "tiled k misaligned": (dict(k=P(1) + 8), MISALIGNED),
+    "block null v": (dict(mapping=0, v=None), INVALID),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MAPPED_CASES))
+def test_record_mapped_rejects(lib, name):
+    kw, want = MAPPED_CASES[name]
+    assert rec_mapped(lib, **kw) == want
+    assert lib.gdn_last_error().decode().startswith("gdn_step_record_mapped")
+
+
+PER_SEQ_CASES = {
+    "null accepted": (dict(accepted=None), INVALID),
+    "accepted misaligned": (dict(accepted=P(5) + 2), MISALIGNED),
+    "T=0": (dict(T=0), INVALID),
+    "null g_log": (dict(g_log=None), INVALID),
+    "Dk=48": (dict(Dk=48), UNSUPPORTED),
+    "state overlap": (dict(state_out=P(3) + 32), INVALID),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PER_SEQ_CASES))
+def test_replay_per_seq_rejects(lib, name):
+    kw, want = PER_SEQ_CASES[name]
+    assert rep_seq(lib, **kw) == want
+    assert lib.gdn_last_error().decode().startswith("gdn_state_replay_per_seq")
 
 
 REPLAY_CASES = {

@@ -326,3 +326,85 @@ def test_repeat_bit_exact(dev, dtype):
     got = gdn.gqa_repeat_tiled(view, 6)
     want = oracle.repeat_tiled(src[1:].reshape(6, 2, 8), 6)
     np.testing.assert_array_equal(storage_of(got), want)
+
+
+# ------------------------------------------------------------ tiled GQA mapping
+def _run_record_tiled(case, dev):
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    out = _alloc_outputs(case, dev)
+    gdn.gdn_step_record(q, k, v, g, beta, s0, mask, gqa="tiled", **out)
+    torch.cuda.synchronize()
+    return out, s0, mask
+
+
+TILED_SPECS = [
+    dict(B=2, T=16, Hk=2, Hv=6, Dk=128, Dv=72, dtype="bf16", mask="bernoulli:0.7", seed=601),
+    dict(B=2, T=7, Hk=4, Hv=8, Dk=64, Dv=40, dtype="bf16", mask="prefix", seed=602),
+    dict(B=2, T=37, Hk=2, Hv=4, Dk=64, Dv=128, dtype="bf16", mask="none", seed=603),
+    dict(B=3, T=21, Hk=2, Hv=4, Dk=128, Dv=33, dtype="f32", mask="none", seed=604),
+    dict(B=1, T=19, Hk=3, Hv=6, Dk=256, Dv=16, dtype="f16", mask="bernoulli:0.5", seed=605),
+    dict(B=2, T=5, Hk=1, Hv=3, Dk=32, Dv=7, dtype="f32", mask="all_on", seed=606),
+]
+
+
+@pytest.mark.parametrize("spec", TILED_SPECS,
+                         ids=lambda s: f"{s['dtype']}-Dk{s['Dk']}-T{s['T']}-Hk{s['Hk']}Hv{s['Hv']}")
+def test_tiled_gqa_mapping(dev, spec):
+    """gdn_step_record_mapped(GDN_GQA_TILED): key head hv % Hk, read in place."""
+    case = workloads.make_case(**spec)
+    got, s0, mask = _run_record_tiled(case, dev)
+    ref = oracle.record(*_oracle_inputs(case), gqa="tiled")
+    _check_record(case, got, ref)
+
+
+def test_long_prefill_fused_tiled_mapping(dev):
+    """The long-prefill workload with the tiled mapping read in place equals,
+    bit for bit, the materialised repeat (16 -> 32 heads) followed by record,
+    and matches the oracle's tiled record."""
+    case = workloads.make_config("long_prefill_t4096_f32")
+    B, T, Hk, Hv, Dk = case.B, case.T, case.Hk, case.Hv, case.Dk
+    fused, s0, mask = _run_record_tiled(case, dev)
+    qd, kd = to_dev(case.q, dev), to_dev(case.k, dev)
+    qx = gdn.gqa_repeat_tiled(qd.reshape(B * T, Hk, Dk), Hv).reshape(B, T, Hv, Dk)
+    kx = gdn.gqa_repeat_tiled(kd.reshape(B * T, Hk, Dk), Hv).reshape(B, T, Hv, Dk)
+    case_x = workloads.Case(**{**case.__dict__, "Hk": Hv})
+    mat, _, _ = _run_record(case_x, dev, q=qx, k=kx)
+    for name in ("y", "delta_log", "state_out", "k_log", "g_log"):
+        assert torch.equal(fused[name], mat[name]), name
+    ref = oracle.record(*_oracle_inputs(case), gqa="tiled")
+    _check_record(case, fused, ref)
+
+
+# ------------------------------------------------------ per-sequence accepted
+def test_replay_per_sequence(dev):
+    """gdn_state_replay_per_seq: one accepted count per sequence (negative,
+    zero, inside, at and past T), against the oracle on a host-made tape and,
+    bit for bit, against the single-count replay of each sequence."""
+    case = workloads.make_config("rollback_b128_t16_bf16", batch=24)
+    dt, T = case.dtype, case.T
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    ref = oracle.record(*_oracle_inputs(case))
+    tape = round_to(np.nan_to_num(ref["delta_log"]), dt)
+    kl = round_to(np.nan_to_num(ref["k_log"]), dt)
+    gl = round_to(np.nan_to_num(ref["g_log"]), dt)
+    dtape, dkl, dgl = to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev)
+    rng = np.random.default_rng(90)
+    acc = rng.integers(-2, T + 4, size=case.B).astype(np.int32)
+    acc[:5] = [0, T, -1, T + 3, 1]
+    dacc = torch.from_numpy(acc).to(dev)
+    st = gdn.gdn_state_replay(dtape, dkl, dgl, s0, mask, accepted=dacc)
+    ref_st = oracle.replay(workloads.widen(tape, dt), workloads.widen(kl, dt),
+                           workloads.widen(gl, dt), case.f64("state"), case.mask,
+                           accepted=acc.astype(np.int64))
+    assert_close(to_host_f64(st), ref_st, dt, None, "per-sequence replay")
+    clipped = np.clip(acc, 0, T)
+    for a in np.unique(clipped):
+        one = gdn.gdn_state_replay(dtape, dkl, dgl, s0, mask, accepted=int(a))
+        rows = torch.from_numpy(clipped == a).to(dev)
+        assert torch.equal(st[rows], one[rows]), f"accepted={a}"
+    # in place: sequences that accept nothing keep their snapshot
+    s1 = s0.clone()
+    gdn.gdn_state_replay_per_seq(dtape, dkl, dgl, s1, mask, accepted=dacc, state_out=s1)
+    assert torch.equal(s1, st)
+    none = torch.from_numpy(clipped == 0).to(dev)
+    assert torch.equal(s1[none], s0[none])
