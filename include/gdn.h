@@ -12,8 +12,8 @@
  *   row-major DEVICE memory (any pointer the CUDA runtime can dereference
  *   from a kernel).  The library never allocates, frees, copies to the host
  *   or synchronises: it validates its arguments on the host, enqueues one
- *   kernel on `stream` and returns.  Results are ready when the stream has
- *   reached that point.
+ *   kernel on `stream` (gdn_chunk_prefill: two) and returns.  Results are
+ *   ready when the stream has reached that point.
  * - `stream` is a cudaStream_t (the typedef below is the same type);
  *   NULL means the legacy default stream.
  * - Dimensions are int64_t and must be > 0 (a zero or negative dimension is
@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 2
+#define GDN_ABI_VERSION 3
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st *gdn_stream_t;
@@ -137,6 +137,39 @@ gdn_status gdn_step_record_mapped(const void *q, const void *k, const void *v,
                                   int64_t B, int64_t T, int64_t Hk, int64_t Hv,
                                   int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
                                   gdn_dtype dtype, gdn_stream_t stream);
+
+/*
+ * gdn_chunk_prefill -- the record recurrence for long calls, computed in
+ * chunks of 16 steps on the tensor cores.
+ *
+ * Same mathematics, arguments, layouts, mask rule and errors as
+ * gdn_step_record_mapped, with these differences:
+ *   - delta_log, k_log and g_log are optional (NULL: not written); y and
+ *     state_out are required.
+ *   - The chunk form re-associates the sums of the step form (the pages give
+ *     only the step form; the chunk form follows from it algebraically), so
+ *     results agree with the step form to float32 rounding, not bit for bit:
+ *     replaying its tape reproduces state_out to rounding, where a float32
+ *     tape of gdn_step_record replays exactly.
+ *   - It needs a caller-owned DEVICE workspace of at least
+ *     gdn_chunk_prefill_workspace_size(B, T, Hv) bytes, 16-byte aligned
+ *     (too small or NULL: GDN_ERR_INVALID_ARGUMENT).  Its contents on entry
+ *     and exit are irrelevant to the caller; two calls in flight at once
+ *     need two workspaces.
+ * It enqueues two kernels on `stream` (the chunk-local matrices, then the
+ * sequential scan over chunks).
+ */
+size_t gdn_chunk_prefill_workspace_size(int64_t B, int64_t T, int64_t Hv);
+
+gdn_status gdn_chunk_prefill(const void *q, const void *k, const void *v,
+                             const void *g, const void *beta,
+                             const float *state_in, const uint32_t *mask,
+                             void *y, float *state_out, void *delta_log,
+                             void *k_log, void *g_log,
+                             int64_t B, int64_t T, int64_t Hk, int64_t Hv,
+                             int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
+                             void *workspace, size_t workspace_bytes,
+                             gdn_dtype dtype, gdn_stream_t stream);
 
 /*
  * gdn_state_replay -- rebuild the state after an accepted prefix of the tape

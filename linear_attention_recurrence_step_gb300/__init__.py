@@ -14,6 +14,10 @@ Entry points (same names as the C ABI):
   gated_delta_replay.rs", kernel gated_delta_step_record.
 * ``gdn_step_record_mapped`` -- the same with the tiled GQA mapping
   ``hk = hv % Hk`` available (``mapping="tiled"``).
+* ``gdn_chunk_prefill`` -- the record recurrence for long calls in chunks of
+  16 steps on the tensor cores (float32-accurate; optional tape outputs;
+  needs a workspace of ``gdn_chunk_prefill_workspace_size`` bytes, which
+  the binding allocates when none is given).
 * ``gdn_state_replay`` -- re-fold the accepted tape prefix onto a snapshot,
   same page, kernel state_replay.
 * ``gdn_state_replay_per_seq`` -- the same with one accepted count per
@@ -34,6 +38,7 @@ import torch
 from . import _build
 
 __all__ = ["GdnError", "build", "load", "lib_path", "gdn_step_record", "gdn_step_record_mapped",
+           "gdn_chunk_prefill", "gdn_chunk_prefill_workspace_size",
            "gdn_state_replay", "gdn_state_replay_per_seq", "gqa_repeat_tiled", "RecordOutputs",
            "STATUS_NAMES", "DTYPE_CODES", "GQA_MAPPINGS"]
 
@@ -41,7 +46,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
                 3: "GDN_ERR_MISALIGNED", 4: "GDN_ERR_CUDA"}
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 GQA_MAPPINGS = {"block": 0, "tiled": 1}
-EXPORTED = ("gdn_step_record", "gdn_step_record_mapped", "gdn_state_replay",
+EXPORTED = ("gdn_step_record", "gdn_step_record_mapped", "gdn_chunk_prefill",
+            "gdn_chunk_prefill_workspace_size", "gdn_state_replay",
             "gdn_state_replay_per_seq", "gqa_repeat_tiled", "gdn_status_string",
             "gdn_last_error", "gdn_abi_version")
 
@@ -75,6 +81,11 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.gdn_step_record.restype = ctypes.c_int
     lib.gdn_step_record_mapped.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int] * 2 + [_P]
     lib.gdn_step_record_mapped.restype = ctypes.c_int
+    lib.gdn_chunk_prefill.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int, _P, ctypes.c_size_t,
+                                                           ctypes.c_int, _P]
+    lib.gdn_chunk_prefill.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_workspace_size.argtypes = [_I] * 3
+    lib.gdn_chunk_prefill_workspace_size.restype = ctypes.c_size_t
     lib.gdn_state_replay.argtypes = [_P] * 6 + [_I] * 6 + [ctypes.c_int, _P]
     lib.gdn_state_replay.restype = ctypes.c_int
     lib.gdn_state_replay_per_seq.argtypes = [_P] * 6 + [_I] * 5 + [_P, ctypes.c_int, _P]
@@ -194,6 +205,70 @@ def gdn_step_record_mapped(q, k, v, g, beta, state_in, mask=None, *, mapping: st
                            **kw) -> RecordOutputs:
     """``gdn_step_record`` with an explicit GQA mapping ("block" or "tiled")."""
     return gdn_step_record(q, k, v, g, beta, state_in, mask, gqa=mapping, **kw)
+
+
+def gdn_chunk_prefill_workspace_size(B: int, T: int, Hv: int) -> int:
+    """Bytes of device workspace gdn_chunk_prefill needs (0 for invalid sizes)."""
+    return int(load().gdn_chunk_prefill_workspace_size(B, T, Hv))
+
+
+def gdn_chunk_prefill(q, k, v, g, beta, state_in, mask=None, *, y=None, state_out=None,
+                      delta_log=None, k_log=None, g_log=None, write_delta: bool = True,
+                      capture_tape: bool = False, gqa: str = "block", workspace=None,
+                      stream=None) -> RecordOutputs:
+    """The record recurrence in chunks of 16 steps on the tensor cores.
+
+    Same inputs and outputs as ``gdn_step_record`` (float32-accurate, not
+    bit-identical to the step form).  ``write_delta=False`` skips the delta
+    tape; ``workspace`` (a device tensor of at least
+    ``gdn_chunk_prefill_workspace_size(B, T, Hv)`` bytes) is allocated when
+    not given."""
+    if gqa not in GQA_MAPPINGS:
+        raise ValueError(f"gqa must be one of {sorted(GQA_MAPPINGS)}")
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dt, dev = q.dtype, q.device
+    if dt not in DTYPE_CODES:
+        raise ValueError(f"unsupported dtype {dt}")
+    _need(q, "q", (B, T, Hk, Dk), dt, dev)
+    _need(k, "k", (B, T, Hk, Dk), dt, dev)
+    _need(v, "v", (B, T, Hv, Dv), dt, dev)
+    _need(g, "g", (B, T, Hv), dt, dev)
+    _need(beta, "beta", (B, T, Hv), dt, dev)
+    _need(state_in, "state_in", (B, Hv, Dv, Dk), torch.float32, dev)
+    if mask is not None:
+        _need(mask, "mask", (B, T), torch.int32 if mask.dtype == torch.int32 else torch.uint32, dev)
+    if y is None:
+        y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    if delta_log is None and write_delta:
+        delta_log = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    if capture_tape:
+        if k_log is None:
+            k_log = torch.empty((B, T, Hv, Dk), dtype=dt, device=dev)
+        if g_log is None:
+            g_log = torch.empty((B, T, Hv), dtype=dt, device=dev)
+    _need(y, "y", (B, T, Hv, Dv), dt, dev)
+    _need(state_out, "state_out", (B, Hv, Dv, Dk), torch.float32, dev)
+    if delta_log is not None:
+        _need(delta_log, "delta_log", (B, T, Hv, Dv), dt, dev)
+    if k_log is not None:
+        _need(k_log, "k_log", (B, T, Hv, Dk), dt, dev)
+    if g_log is not None:
+        _need(g_log, "g_log", (B, T, Hv), dt, dev)
+    need = gdn_chunk_prefill_workspace_size(B, T, Hv)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    st = load().gdn_chunk_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(mask), _ptr(y),
+        _ptr(state_out), _ptr(delta_log), _ptr(k_log), _ptr(g_log), B, T, Hk, Hv, Dk, Dv,
+        GQA_MAPPINGS[gqa], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        DTYPE_CODES[dt], _stream(dev, stream))
+    _check(st, "gdn_chunk_prefill")
+    return RecordOutputs(y, state_out, delta_log, k_log, g_log)
 
 
 def gdn_state_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted,

@@ -13,6 +13,7 @@
 #include "record.cuh"
 #include "record_mma.cuh"
 #include "replay.cuh"
+#include "chunk.cuh"
 
 namespace {
 
@@ -287,9 +288,88 @@ gdn_status replay_impl(const char *fn, const void *delta_log, const void *k_log,
     return ok();
 }
 
+gdn_status chunk_prefill_impl(const char *fn, const void *q, const void *k, const void *v,
+                              const void *g, const void *beta, const float *state_in,
+                              const uint32_t *mask, void *y, float *state_out, void *delta_log,
+                              void *k_log, void *g_log, int64_t B, int64_t T, int64_t Hk,
+                              int64_t Hv, int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
+                              void *workspace, size_t workspace_bytes, gdn_dtype dtype,
+                              gdn_stream_t stream) {
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dtype);
+    if (mapping != GDN_GQA_BLOCK && mapping != GDN_GQA_TILED)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: unknown GQA mapping %d", fn, (int)mapping);
+    if (B <= 0 || T <= 0 || Hk <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: B, T, Hk, Hv, Dk, Dv must all be > 0 (got %lld %lld %lld %lld %lld %lld)", fn,
+                    (long long)B, (long long)T, (long long)Hk, (long long)Hv, (long long)Dk, (long long)Dv);
+    if (Hv % Hk != 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: Hv (%lld) must be a multiple of Hk (%lld)", fn,
+                    (long long)Hv, (long long)Hk);
+    if (!q || !k || !v || !g || !beta || !state_in || !y || !state_out || !workspace)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: q, k, v, g, beta, state_in, y, state_out, workspace must be non-NULL", fn);
+    if (Dk % 32 != 0 || !gdn::supported_dk(Dk))
+        return fail(GDN_ERR_UNSUPPORTED, "%s: Dk = %lld not supported (32, 64, 128, 192, 256)", fn,
+                    (long long)Dk);
+    const int64_t qk_b = nbytes({B, T, Hk, Dk}, eb), v_b = nbytes({B, T, Hv, Dv}, eb);
+    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), kl_b = nbytes({B, T, Hv, Dk}, eb);
+    const int64_t gb_b = nbytes({B, T, Hv}, eb), m_b = nbytes({B, T}, 4);
+    const int64_t ws_b = gdn::chunk_workspace_bytes(B, T, Hv);
+    if (qk_b < 0 || v_b < 0 || s_b < 0 || kl_b < 0 || gb_b < 0 || m_b < 0 || ws_b < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: tensor sizes overflow int64", fn);
+    if (workspace_bytes < (uint64_t)ws_b)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: workspace too small: need %lld bytes, have %llu", fn,
+                    (long long)ws_b, (unsigned long long)workspace_bytes);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(state_in, 16) || !aligned(state_out, 16) ||
+        !aligned(k_log, 16) || !aligned(workspace, 16))
+        return fail(GDN_ERR_MISALIGNED,
+                    "%s: q, k, state_in, state_out, k_log, workspace must be 16-byte aligned", fn);
+    if (!aligned(v, eb) || !aligned(g, eb) || !aligned(beta, eb) || !aligned(y, eb) ||
+        !aligned(delta_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4))
+        return fail(GDN_ERR_MISALIGNED, "%s: a tensor is not aligned to its element size", fn);
+    if (state_in != state_out && overlap(state_in, s_b, state_out, s_b))
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: state_out overlaps state_in without being the same buffer", fn);
+
+    gdn::ChunkArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+    a.state_in = state_in; a.mask = mask; a.y = y; a.state_out = state_out;
+    a.delta_log = delta_log; a.k_log = k_log; a.g_log = g_log;
+    a.workspace = static_cast<float *>(workspace);
+    a.B = B; a.T = T; a.Hk = Hk; a.Hv = Hv; a.Dv = Dv;
+    a.nchunks = ceil_div(T, gdn::kCkC);
+    a.row_blocks = ceil_div(Dv, gdn::kCkRows);
+    a.vec_v = aligned(v, 16) && (Dv * eb) % 16 == 0;
+    a.tiled_gqa = mapping == GDN_GQA_TILED;
+    if ((B * Hv) > (int64_t)INT32_MAX / a.nchunks || (B * Hv) > (int64_t)INT32_MAX / a.row_blocks)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large", fn);
+    const cudaError_t e = gdn::launch_chunk(static_cast<gdn::DType>(dtype), (int)Dk, a,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(fn, "launch", e);
+    return ok();
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t gdn_chunk_prefill_workspace_size(int64_t B, int64_t T, int64_t Hv) {
+    if (B <= 0 || T <= 0 || Hv <= 0) return 0;
+    const int64_t r = gdn::chunk_workspace_bytes(B, T, Hv);
+    return r < 0 ? 0 : (size_t)r;
+}
+
+gdn_status gdn_chunk_prefill(const void *q, const void *k, const void *v, const void *g,
+                             const void *beta, const float *state_in, const uint32_t *mask,
+                             void *y, float *state_out, void *delta_log, void *k_log,
+                             void *g_log, int64_t B, int64_t T, int64_t Hk, int64_t Hv,
+                             int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping, void *workspace,
+                             size_t workspace_bytes, gdn_dtype dtype, gdn_stream_t stream) {
+    return chunk_prefill_impl("gdn_chunk_prefill", q, k, v, g, beta, state_in, mask, y, state_out,
+                              delta_log, k_log, g_log, B, T, Hk, Hv, Dk, Dv, mapping, workspace,
+                              workspace_bytes, dtype, stream);
+}
 
 gdn_status gdn_step_record(const void *q, const void *k, const void *v, const void *g,
                            const void *beta, const float *state_in, const uint32_t *mask,

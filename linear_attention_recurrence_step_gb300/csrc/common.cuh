@@ -13,6 +13,9 @@
 
 namespace gdn {
 
+// Round a byte count up to a multiple of 16 (shared-memory carving).
+__host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
 // ------------------------------------------------------------ element types
 template <typename T> struct Elem;
 

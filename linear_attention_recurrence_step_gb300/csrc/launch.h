@@ -52,6 +52,23 @@ struct ReplayArgs {
                            // min(max(acc_b[b], 0), steps) steps
 };
 
+// Chunked prefill (chunk.cuh): record semantics over chunks of 16 steps,
+// with a caller-provided workspace for the chunk-local matrices.
+struct ChunkArgs {
+    const void *q, *k, *v, *g, *beta;
+    const float *state_in;
+    const uint32_t *mask;
+    void *y;
+    float *state_out;
+    void *delta_log, *k_log, *g_log;  // delta_log, k_log, g_log may be null
+    float *workspace;                 // [B, Hv, nchunks, 544] f32
+    int64_t B, T, Hk, Hv, Dv;
+    int64_t nchunks;     // ceil(T / 16)
+    int64_t row_blocks;  // ceil(Dv / 16)
+    bool vec_v;          // v rows can be copied in 16-byte pieces
+    bool tiled_gqa;      // key head hv % Hk instead of hv / (Hv/Hk)
+};
+
 struct RepeatArgs {
     const void *src;
     void *dst;
@@ -76,5 +93,7 @@ cudaError_t launch_record_f16(int dk, const RecordArgs &a, const Geometry &geo, 
 cudaError_t launch_replay(DType dt, int dk, const ReplayArgs &a, const Geometry &geo,
                           cudaStream_t s);
 cudaError_t launch_repeat(const RepeatArgs &a, cudaStream_t s, int sm_count);
+cudaError_t launch_chunk(DType dt, int dk, const ChunkArgs &a, cudaStream_t s);
+int64_t chunk_workspace_bytes(int64_t B, int64_t T, int64_t Hv);  // -1 on overflow
 
 }  // namespace gdn

@@ -28,7 +28,6 @@
 
 namespace gdn {
 
-__host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
 // Shared memory of the record kernel (bytes), in carve order:
 //   raw ring   2 x { K[tc][dk], Q[tc][dk], V[tc][rows] }   element type

@@ -44,7 +44,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for want in ("gdn_step_record", "gdn_step_record_mapped", "gdn_state_replay",
+    for want in ("gdn_step_record", "gdn_step_record_mapped", "gdn_chunk_prefill",
+                 "gdn_chunk_prefill_workspace_size", "gdn_state_replay",
                  "gdn_state_replay_per_seq", "gqa_repeat_tiled",
                  "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
         assert want in names
@@ -54,7 +55,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libgdn.so does not export {name}"
-    assert lib.gdn_abi_version() == 2
+    assert lib.gdn_abi_version() == 3
 
 
 def test_library_is_sm103a():
@@ -91,6 +92,49 @@ def rec_mapped(lib, mapping=1, **kw):
                 B=2, T=3, Hk=2, Hv=4, Dk=64, Dv=32, mapping=mapping, dtype=BF16, stream=None)
     args.update(kw)
     return lib.gdn_step_record_mapped(*args.values())
+
+
+def chunk(lib, **kw):
+    ws = lib.gdn_chunk_prefill_workspace_size(2, 3, 4)
+    args = dict(q=P(0), k=P(1), v=P(2), g=P(3), beta=P(4), state_in=P(5), mask=None,
+                y=P(6), state_out=P(7), delta_log=None, k_log=None, g_log=None,
+                B=2, T=3, Hk=2, Hv=4, Dk=64, Dv=32, mapping=0, workspace=P(9),
+                workspace_bytes=ws, dtype=F32, stream=None)
+    args.update(kw)
+    return lib.gdn_chunk_prefill(*args.values())
+
+
+def test_chunk_workspace_size(lib):
+    # one block of 2 x 16 x 16 + 2 x 16 floats per (b, hv, 16-step chunk)
+    assert lib.gdn_chunk_prefill_workspace_size(1, 4096, 32) == 32 * 256 * 544 * 4
+    assert lib.gdn_chunk_prefill_workspace_size(2, 17, 3) == 2 * 3 * 2 * 544 * 4
+    assert lib.gdn_chunk_prefill_workspace_size(0, 5, 5) == 0
+    assert lib.gdn_chunk_prefill_workspace_size(1 << 40, 1 << 30, 64) == 0
+
+
+CHUNK_CASES = {
+    "null workspace": (dict(workspace=None), INVALID),
+    "workspace too small": (dict(workspace_bytes=100), INVALID),
+    "workspace misaligned": (dict(workspace=P(9) + 8), MISALIGNED),
+    "mapping=3": (dict(mapping=3), INVALID),
+    "null y": (dict(y=None), INVALID),
+    "T=0": (dict(T=0), INVALID),
+    "Hv%Hk": (dict(Hk=3), INVALID),
+    "Dk=80": (dict(Dk=80), UNSUPPORTED),
+    "dtype": (dict(dtype=7), UNSUPPORTED),
+    "q misaligned": (dict(q=P(0) + 4), MISALIGNED),
+    "state overlap": (dict(state_out=P(5) + 16), INVALID),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHUNK_CASES))
+def test_chunk_prefill_rejects(lib, name):
+    kw, want = CHUNK_CASES[name]
+    assert chunk(lib, **kw) == want
+    msg = lib.gdn_last_error().decode()
+    assert msg.startswith("gdn_chunk_prefill")
+    if name == "workspace too small":
+        assert "need 17408 bytes, have 100" in msg  # 2 x 4 x 1 x 544 x 4
 
 
 def rep_seq(lib, **kw):

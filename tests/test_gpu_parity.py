@@ -408,3 +408,107 @@ def test_replay_per_sequence(dev):
     assert torch.equal(s1, st)
     none = torch.from_numpy(clipped == 0).to(dev)
     assert torch.equal(s1[none], s0[none])
+
+
+# ------------------------------------------------------------ chunked prefill
+def _run_chunk(case, dev, gqa="block", capture=True, write_delta=True):
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    out = _alloc_outputs(case, dev, capture)
+    if not write_delta:
+        out.pop("delta_log")
+    gdn.gdn_chunk_prefill(q, k, v, g, beta, s0, mask, gqa=gqa, write_delta=write_delta, **out)
+    torch.cuda.synchronize()
+    return out, s0, mask
+
+
+CHUNK_SPECS = [
+    dict(B=1, T=1, Hk=1, Hv=1, Dk=32, Dv=16, dtype="f32", mask="none", seed=701),
+    dict(B=2, T=15, Hk=2, Hv=4, Dk=64, Dv=40, dtype="f32", mask="bernoulli:0.6", seed=702),
+    dict(B=2, T=16, Hk=1, Hv=2, Dk=128, Dv=128, dtype="f32", mask="none", seed=703),
+    dict(B=1, T=100, Hk=2, Hv=4, Dk=128, Dv=33, dtype="f32", mask="prefix", seed=704),
+    dict(B=2, T=37, Hk=3, Hv=6, Dk=192, Dv=20, dtype="f32", mask="bernoulli:0.8", seed=705),
+    dict(B=1, T=50, Hk=1, Hv=2, Dk=256, Dv=48, dtype="f32", mask="none", seed=706),
+    dict(B=2, T=33, Hk=2, Hv=4, Dk=128, Dv=64, dtype="bf16", mask="bernoulli:0.7", seed=707),
+    dict(B=1, T=64, Hk=4, Hv=8, Dk=64, Dv=17, dtype="f16", mask="none", seed=708),
+    dict(B=3, T=20, Hk=1, Hv=1, Dk=32, Dv=5, dtype="bf16", mask="all_off", seed=709),
+]
+
+
+@pytest.mark.parametrize("spec", CHUNK_SPECS,
+                         ids=lambda s: f"{s['dtype']}-Dk{s['Dk']}-Dv{s['Dv']}-T{s['T']}-{s['mask']}")
+def test_chunk_prefill(dev, spec):
+    """gdn_chunk_prefill against the oracle's step-form record: ragged chunks
+    (T = 1, 15, 16, 33, 37, 100), ragged row blocks, every Dk, every dtype,
+    masks (inactive steps write nothing), tape capture."""
+    case = workloads.make_case(**spec)
+    got, s0, mask = _run_chunk(case, dev)
+    ref = oracle.record(*_oracle_inputs(case))
+    _check_record(case, got, ref)
+
+
+def test_chunk_prefill_long_tiled(dev):
+    """The long-prefill workload (T = 4096, f32, 16 key heads read in place
+    by 32 value heads with the tiled mapping) against the oracle."""
+    case = workloads.make_config("long_prefill_t4096_f32")
+    got, s0, mask = _run_chunk(case, dev, gqa="tiled", capture=False)
+    ref = oracle.record(*_oracle_inputs(case), gqa="tiled", capture_tape=False)
+    _check_record(case, got, ref, capture=False)
+
+
+def test_chunk_prefill_decay_edges(dev):
+    """g = 0 resets, long runs of small g (products far below f32's range),
+    and growth g in (2, 3) held to 1e-4 of each row's largest entry (f32's own
+    limit under growth, as for the step form)."""
+    for seed, T, g_range in [(21, 40, (0.0, 0.0)), (22, 80, (0.0, 0.3)), (23, 300, (0.6, 1.0))]:
+        case = workloads.make_case(B=2, T=T, Hk=1, Hv=2, Dk=64, Dv=40, dtype="f32", seed=seed,
+                                   g_range=g_range, mask="bernoulli:0.9")
+        got, s0, mask = _run_chunk(case, dev)
+        ref = oracle.record(*_oracle_inputs(case))
+        _check_record(case, got, ref)
+    case = workloads.make_case(B=2, T=36, Hk=1, Hv=2, Dk=64, Dv=40, dtype="f32", seed=24,
+                               g_range=(2.0, 3.0), mask="bernoulli:0.9")
+    got, s0, mask = _run_chunk(case, dev)
+    ref = oracle.record(*_oracle_inputs(case))
+    st = to_host_f64(got["state_out"])
+    row_scale = np.abs(ref["state_out"]).max(axis=-1, keepdims=True)
+    assert (np.abs(st - ref["state_out"]) <= 1e-4 * row_scale).all()
+
+
+def test_chunk_prefill_ignores_masked_inputs(dev):
+    """NaN in the q / k / v / g / beta slots of masked steps never reaches
+    the outputs (the chunk products multiply those rows by zero)."""
+    case = workloads.make_case(B=2, T=40, Hk=2, Hv=4, Dk=128, Dv=48, dtype="f32", seed=25,
+                               mask="bernoulli:0.6")
+    clean, s0, mask = _run_chunk(case, dev)
+    off = ~case.mask.astype(bool)
+    dirty_case = workloads.Case(**case.__dict__)
+    for name in ("q", "k", "v", "g", "beta"):
+        arr = getattr(case, name).copy()
+        arr[off] = np.nan
+        setattr(dirty_case, name, arr)
+    dirty, _, _ = _run_chunk(dirty_case, dev)
+    on = torch.from_numpy(case.mask.astype(bool)).to(dev)
+    assert torch.equal(dirty["state_out"], clean["state_out"])
+    assert torch.equal(dirty["y"][on], clean["y"][on])
+    assert torch.equal(dirty["delta_log"][on], clean["delta_log"][on])
+
+
+def test_chunk_prefill_tape_and_in_place(dev):
+    """Replaying the chunk form's own float32 tape lands on its state_out (to
+    rounding); the in-place call equals the out-of-place one; skipping the
+    delta tape changes nothing else."""
+    case = workloads.make_case(B=2, T=70, Hk=2, Hv=4, Dk=128, Dv=64, dtype="f32", seed=26,
+                               mask="bernoulli:0.8")
+    got, s0, mask = _run_chunk(case, dev)
+    st = gdn.gdn_state_replay(got["delta_log"], got["k_log"], got["g_log"], s0, mask,
+                              accepted=case.T)
+    assert_close(to_host_f64(st), to_host_f64(got["state_out"]), "f32", None, "replay of chunk tape")
+    q, k, v, g, beta, _, _ = device_inputs(case, dev)
+    s1 = s0.clone()
+    gdn.gdn_chunk_prefill(q, k, v, g, beta, s1, mask, state_out=s1)
+    torch.cuda.synchronize()
+    assert torch.equal(s1, got["state_out"])
+    nodelta, _, _ = _run_chunk(case, dev, capture=False, write_delta=False)
+    on = torch.from_numpy(case.mask.astype(bool)).to(dev)
+    assert torch.equal(nodelta["state_out"], got["state_out"])
+    assert torch.equal(nodelta["y"][on], got["y"][on])
