@@ -4,8 +4,8 @@
 // tensor cores (warp-level mma.sync, tf32 operands, f32 accumulate), in
 // float32 accuracy.
 //
-// Within a chunk (steps 0..C-1 after the chunk's first step, state s_in at
-// entry, inactive steps given g = 1 and beta = 0) the step
+// Within a chunk (steps 0..C-1, state s_in at entry, inactive steps given
+// g = 1 and beta = 0) the step
 //     s <- g s;  delta = beta (v - s.k);  s <- s + k delta;  y = s.q
 // unrolls, with Gam_t = prod_{x<=t} g_x and A[t][u] = prod_{u<x<=t} g_x, to
 //     (I + N) delta = r,   N[t][u] = beta_t A[t][u] (k_u.k_t)   (u < t)
@@ -17,17 +17,18 @@
 // with beta folded in (Wb[t][u] = W[t][u] beta_u), Mq[t][u] = A[t][u]
 // (k_u.q_t), Gam, aC[u] = A[C-1][u] -- is computed for every (b, hv, chunk)
 // at once by chunk_local_kernel into a caller-provided workspace.  The
-// sequential part, chunk_scan_kernel, then walks the chunks of one tile's row
+// sequential part, chunk_scan_kernel, walks the chunks of one tile's row
 // block with four MMA products per chunk:
-//     P  = S_in [Gam K ; Gam Q]^T     (rows x 2C, contraction over Dk)
+//     P  = S_in [K ; Q]^T, then scaled by Gam per step (rows x 2C, over Dk)
 //     D  = (V^T - P_k) Wb^T           (the deltas, contraction over C)
 //     Y  = P_q + D Mq^T               (contraction over C)
-//     S  = Gam_{C-1} S_in + D (aC K)  (rows x Dk, contraction over C)
+//     S  = Gam_{C-1} S_in + (D aC) K  (rows x Dk, contraction over C)
 //
 // Accuracy: every product runs as three tf32 MMAs (a_hi b_lo + a_lo b_hi +
-// a_hi b_hi, each operand split x = hi + lo with hi = tf32(x)), which keeps
-// about 21 significant bits per product and f32 accumulation; the state stays
-// f32 in the accumulator fragments for the whole launch.
+// a_hi b_hi, each operand split x = hi + lo with hi = x rounded to tf32 and
+// lo = x - hi exact in f32), about 21 significant bits per product with f32
+// accumulation; the state stays f32 in the accumulator fragments for the
+// whole launch.
 //
 // Work split: a CTA owns 16 state rows of one (b, hv) tile and four warps
 // split the Dk columns (each holds 16 rows x Dk/4 of the state).  The partial
@@ -48,10 +49,12 @@ namespace gdn {
 
 constexpr int kCkC = 16;           // timesteps per chunk
 constexpr int kCkWarps = 4;        // warps per scan CTA (Dk split four ways)
+constexpr int kCkThreads = 32 * kCkWarps;
 constexpr int kCkRows = 16;        // state rows per scan CTA
 constexpr int kCkLocalThreads = 256;
 constexpr int kCkWsFloats = 2 * kCkC * kCkC + 2 * kCkC;  // Wb, Mq, Gam, aC per (b, hv, chunk)
 constexpr int kCkPartStride = 40;  // floats per row of a partial-product block (32 + pad)
+constexpr int kCkOutStride = 20;   // floats per step row of the y / delta staging tile
 
 __host__ __device__ constexpr int ck_kstride(int dk) { return dk + 8; }  // padded k / q row (elements)
 __host__ __device__ constexpr int ck_vstride(int esize) { return kCkRows + 16 / esize; }
@@ -62,23 +65,22 @@ __host__ __device__ constexpr size_t ck_slot_bytes(int dk, int esize) {
 }
 __host__ __device__ constexpr size_t chunk_scan_smem_bytes(int dk, int esize) {
     return 3 * ck_slot_bytes(dk, esize) +
-           (size_t)2 * kCkWarps * kCkRows * kCkPartStride * 4;
+           (size_t)2 * kCkWarps * kCkRows * kCkPartStride * 4 +
+           (size_t)2 * kCkC * kCkOutStride * 4;
 }
 __host__ __device__ constexpr size_t chunk_local_smem_bytes(int dk) {
-    return (size_t)2 * kCkC * (dk + 1) * 4 + (size_t)4 * kCkC * (kCkC + 1) * 4 +
+    return (size_t)2 * kCkC * (dk + 4) * 4 + (size_t)4 * kCkC * (kCkC + 1) * 4 +
            (size_t)3 * kCkC * 4;
 }
 
 // ------------------------------------------------------------ tf32 products
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
-    return r;
-}
-// x ~ hi + lo, both tf32; x - hi is exact in f32.
+// x ~ hi + lo: hi = x rounded to tf32 (nearest, ties away: add half a tf32
+// ulp to the bits, clear the 13 low bits), lo = x - hi exactly.  lo goes to
+// the MMA as is; the tensor core reads its tf32 part (19 high bits), which
+// leaves |error| < 2^-21 |x|.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = tf32_rna(x);
-    lo = tf32_rna(x - __uint_as_float(hi));
+    hi = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
 }
 __device__ __forceinline__ void mma_tf32_1688(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                               uint32_t b1) {
@@ -124,32 +126,89 @@ __device__ __forceinline__ float2 ld2f<__half>(const __half *p) {
     return __half22float2(*reinterpret_cast<const __half2 *>(p));
 }
 
+// Four consecutive values stored as T (16 bytes of f32, 8 of bf16 / f16).
+template <typename T>
+__device__ __forceinline__ void st4(T *p, float4 v);
+template <>
+__device__ __forceinline__ void st4<float>(float *p, float4 v) {
+    *reinterpret_cast<float4 *>(p) = v;
+}
+template <>
+__device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&a);
+    u.y = *reinterpret_cast<const uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+template <>
+__device__ __forceinline__ void st4<__half>(__half *p, float4 v) {
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&a);
+    u.y = *reinterpret_cast<const uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+// One 16-byte piece of T widened to f32 (exact).
+template <typename T>
+__device__ __forceinline__ void widen_piece(uint4 raw, float (&out)[16 / sizeof(T)]);
+template <>
+__device__ __forceinline__ void widen_piece<float>(uint4 raw, float (&out)[4]) {
+    out[0] = __uint_as_float(raw.x);
+    out[1] = __uint_as_float(raw.y);
+    out[2] = __uint_as_float(raw.z);
+    out[3] = __uint_as_float(raw.w);
+}
+template <>
+__device__ __forceinline__ void widen_piece<__nv_bfloat16>(uint4 raw, float (&out)[8]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void widen_piece<__half>(uint4 raw, float (&out)[8]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+        out[2 * i] = f.x;
+        out[2 * i + 1] = f.y;
+    }
+}
+
 // ------------------------------------------------------------ chunk-local part
-// One CTA per (b, hv, chunk): Gram products, decay products, the unit
-// lower-triangular inverse, and the tape capture of k_log / g_log.
+// One CTA per (b, hk, chunk): the Gram products of key head hk (shared by the
+// G value heads that read it), then for each of those value heads the decay
+// products, the unit lower-triangular inverse, the workspace block and the
+// tape capture of k_log / g_log.
 template <typename TIn, int DK>
 __global__ void __launch_bounds__(kCkLocalThreads)
 chunk_local_kernel(const ChunkArgs a) {
     constexpr int C = kCkC;
-    constexpr int KS = DK + 1;   // f32 row stride: row u of a warp lands on bank u
+    constexpr int KS = DK + 4;   // f32 row stride: float4 rows u land 4 banks apart
     constexpr int CS = C + 1;
+    constexpr int VEC = 16 / (int)sizeof(TIn);
     extern __shared__ __align__(16) unsigned char smem[];
     float *sk = reinterpret_cast<float *>(smem);
     float *sq = sk + C * KS;
-    float *sA = sq + C * KS;     // A[t][u], u <= t
-    float *sKK = sA + C * CS;    // k_t . k_u
+    float *sKK = sq + C * KS;    // k_t . k_u
     float *sKQ = sKK + C * CS;   // k_u . q_t
-    float *sW = sKQ + C * CS;    // W = (I + N)^-1
-    float *sg = sW + C * CS;     // effective g (1 on inactive steps)
+    float *sA = sKQ + C * CS;    // A[t][u], u <= t (zero above)
+    float *sN = sA + C * CS;     // N[t][u], u < t (zero elsewhere)
+    float *sg = sN + C * CS;     // effective g (1 on inactive steps)
     float *sb = sg + C;          // effective beta (0 on inactive steps)
     float *sG = sb + C;          // Gam_t
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int64_t nch = a.nchunks;
-    const int64_t n = blockIdx.x / nch;
-    const int64_t c = blockIdx.x - n * nch;
-    const int64_t b = n / a.Hv, hv = n - b * a.Hv;
-    const int64_t hk = a.tiled_gqa ? hv % a.Hk : hv / (a.Hv / a.Hk);
+    const int64_t m = blockIdx.x / nch;          // b * Hk + hk
+    const int64_t c = blockIdx.x - m * nch;
+    const int64_t b = m / a.Hk, hk = m - b * a.Hk;
+    const int64_t G = a.Hv / a.Hk;
     const int64_t t0 = c * C;
     const int tcnt = (int)min((int64_t)C, a.T - t0);
     const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
@@ -160,108 +219,125 @@ chunk_local_kernel(const ChunkArgs a) {
     const TIn *bp = static_cast<const TIn *>(a.beta);
 
     // k / q rows of active steps, widened; rows of inactive steps are zero
-    for (int i = tid; i < C * DK; i += kCkLocalThreads) {
-        const int tt = i / DK, x = i - tt * DK;
-        float kv = 0.f, qv = 0.f;
+    for (int i = tid; i < C * DK / VEC; i += kCkLocalThreads) {
+        const int tt = i / (DK / VEC), x = (i - tt * (DK / VEC)) * VEC;
+        float kv[VEC], qv[VEC];
         if ((bits >> tt) & 1u) {
             const int64_t off = ((b * a.T + t0 + tt) * a.Hk + hk) * DK + x;
-            kv = ld_f32(kp + off);
-            qv = ld_f32(qp + off);
+            widen_piece<TIn>(*reinterpret_cast<const uint4 *>(kp + off), kv);
+            widen_piece<TIn>(*reinterpret_cast<const uint4 *>(qp + off), qv);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) kv[e] = qv[e] = 0.f;
         }
-        sk[tt * KS + x] = kv;
-        sq[tt * KS + x] = qv;
-    }
-    if (tid < C) {
-        const bool on = (bits >> tid) & 1u;
-        const int64_t gi = (b * a.T + t0 + tid) * a.Hv + hv;
-        sg[tid] = on ? ld_f32(gp + gi) : 1.f;
-        sb[tid] = on ? ld_f32(bp + gi) : 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4) {
+            *reinterpret_cast<float4 *>(sk + tt * KS + x + e) = make_float4(kv[e], kv[e + 1], kv[e + 2], kv[e + 3]);
+            *reinterpret_cast<float4 *>(sq + tt * KS + x + e) = make_float4(qv[e], qv[e + 1], qv[e + 2], qv[e + 3]);
+        }
     }
     __syncthreads();
 
-    // one (t, u) pair per thread: Gram entries and the decay product A[t][u]
+    // Gram entries, one (t, u) pair per thread
     {
         const int t = tid >> 4, u = tid & 15;
         float kk = 0.f, kq = 0.f;
-#pragma unroll 8
-        for (int x = 0; x < DK; ++x) {
-            const float ku = sk[u * KS + x];
-            kk = fmaf(sk[t * KS + x], ku, kk);
-            kq = fmaf(sq[t * KS + x], ku, kq);
+#pragma unroll 4
+        for (int x = 0; x < DK; x += 4) {
+            const float4 ku = *reinterpret_cast<const float4 *>(sk + u * KS + x);
+            const float4 kt = *reinterpret_cast<const float4 *>(sk + t * KS + x);
+            const float4 qt = *reinterpret_cast<const float4 *>(sq + t * KS + x);
+            kk = fmaf(kt.x, ku.x, fmaf(kt.y, ku.y, fmaf(kt.z, ku.z, fmaf(kt.w, ku.w, kk))));
+            kq = fmaf(qt.x, ku.x, fmaf(qt.y, ku.y, fmaf(qt.z, ku.z, fmaf(qt.w, ku.w, kq))));
         }
         sKK[t * CS + u] = kk;
         sKQ[t * CS + u] = kq;
-        float p = 1.f;
-        for (int x = u + 1; x <= t; ++x) p *= sg[x];
-        sA[t * CS + u] = u <= t ? p : 0.f;
-        if (u == 0) {
-            float G = 1.f;
-            for (int x = 0; x <= t; ++x) G *= sg[x];
-            sG[t] = G;
-        }
     }
-    __syncthreads();
 
-    // W = (I + N)^-1 by forward substitution, one column u per thread:
-    // W[t][u] = -sum_{u <= x < t} N[t][x] W[x][u],  N[t][x] = beta_t A[t][x] KK[t][x]
-    if (tid < C) {
-        const int u = tid;
-        for (int t = 0; t < C; ++t) {
-            float w;
-            if (t < u) {
-                w = 0.f;
-            } else if (t == u) {
-                w = 1.f;
-            } else {
-                float acc = 0.f;
-                for (int x = u; x < t; ++x)
-                    acc = fmaf(sb[t] * sA[t * CS + x] * sKK[t * CS + x], sW[x * CS + u], acc);
-                w = -acc;
+    for (int64_t i = 0; i < G; ++i) {
+        const int64_t hv = a.tiled_gqa ? hk + i * a.Hk : hk * G + i;
+        const int64_t n = b * a.Hv + hv;
+        if (tid < C) {
+            const bool on = (bits >> tid) & 1u;
+            const int64_t gi = (b * a.T + t0 + tid) * a.Hv + hv;
+            sg[tid] = on ? ld_f32(gp + gi) : 1.f;
+            sb[tid] = on ? ld_f32(bp + gi) : 0.f;
+        }
+        __syncthreads();  // g, beta of this head; Gram entries (first pass)
+        {
+            const int t = tid >> 4, u = tid & 15;
+            float p = 1.f;
+            for (int x = u + 1; x <= t; ++x) p *= sg[x];
+            sA[t * CS + u] = u <= t ? p : 0.f;
+            sN[t * CS + u] = u < t ? sb[t] * p * sKK[t * CS + u] : 0.f;
+            if (u == 0) {
+                float Gm = 1.f;
+                for (int x = 0; x <= t; ++x) Gm *= sg[x];
+                sG[t] = Gm;
             }
-            sW[t * CS + u] = w;
         }
-    }
-    __syncthreads();
+        __syncthreads();
 
-    float *ws = a.workspace + (n * nch + c) * kCkWsFloats;
-    {
-        const int t = tid >> 4, u = tid & 15;
-        ws[t * C + u] = u <= t ? sW[t * CS + u] * sb[u] : 0.f;            // Wb
-        ws[C * C + t * C + u] = u <= t ? sA[t * CS + u] * sKQ[t * CS + u] : 0.f;  // Mq
-        if (tid < C) ws[2 * C * C + tid] = sG[tid];                        // Gam
-        if (tid < C) ws[2 * C * C + C + tid] = sA[(C - 1) * CS + tid];     // aC
-    }
-
-    // tape capture: k_log rows and g_log of the active steps
-    if (a.k_log) {
-        TIn *klp = static_cast<TIn *>(a.k_log);
-        for (int i = tid; i < C * DK; i += kCkLocalThreads) {
-            const int tt = i / DK, x = i - tt * DK;
-            if ((bits >> tt) & 1u)
-                klp[((b * a.T + t0 + tt) * a.Hv + hv) * DK + x] =
-                    kp[((b * a.T + t0 + tt) * a.Hk + hk) * DK + x];
+        float *ws = a.workspace + (n * nch + c) * kCkWsFloats;
+        if (tid < C) {
+            // W = (I + N)^-1, one column u per thread, held in registers:
+            // W[t][u] = -sum_{x < t} N[t][x] W[x][u]  (W[x][u] = 0 for x < u)
+            const int u = tid;
+            float w[C];
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                float acc = 0.f;
+#pragma unroll
+                for (int x = 0; x < t; ++x) acc = fmaf(sN[t * CS + x], w[x], acc);
+                w[t] = t < u ? 0.f : (t == u ? 1.f : -acc);
+            }
+            const float bu = sb[u];
+#pragma unroll
+            for (int t = 0; t < C; ++t) ws[t * C + u] = w[t] * bu;  // Wb
+        } else {
+            for (int j = tid - C; j < C * C; j += kCkLocalThreads - C) {
+                const int t = j >> 4, u = j & 15;
+                ws[C * C + j] = u <= t ? sA[t * CS + u] * sKQ[t * CS + u] : 0.f;  // Mq
+            }
+            if (tid >= 2 * C && tid < 3 * C) ws[2 * C * C + tid - 2 * C] = sG[tid - 2 * C];      // Gam
+            if (tid >= 3 * C && tid < 4 * C) ws[2 * C * C + C + tid - 3 * C] = sA[(C - 1) * CS + tid - 3 * C];  // aC
+            // tape capture: k_log rows and g_log of the active steps
+            if (a.k_log) {
+                TIn *klp = static_cast<TIn *>(a.k_log);
+                for (int j = tid - C; j < C * DK / VEC; j += kCkLocalThreads - C) {
+                    const int tt = j / (DK / VEC), x = (j - tt * (DK / VEC)) * VEC;
+                    if ((bits >> tt) & 1u)
+                        *reinterpret_cast<uint4 *>(klp + ((b * a.T + t0 + tt) * a.Hv + hv) * DK + x) =
+                            *reinterpret_cast<const uint4 *>(kp + ((b * a.T + t0 + tt) * a.Hk + hk) * DK + x);
+                }
+            }
+            if (a.g_log && tid >= C && tid < C + tcnt && ((bits >> (tid - C)) & 1u)) {
+                const int64_t gi = (b * a.T + t0 + tid - C) * a.Hv + hv;
+                static_cast<TIn *>(a.g_log)[gi] = gp[gi];
+            }
         }
-    }
-    if (a.g_log && tid < tcnt && ((bits >> tid) & 1u)) {
-        const int64_t gi = (b * a.T + t0 + tid) * a.Hv + hv;
-        static_cast<TIn *>(a.g_log)[gi] = gp[gi];
+        __syncthreads();  // sg / sb / sA / sN are rewritten for the next head
     }
 }
 
 // ------------------------------------------------------------ sequential part
 template <typename TIn, int DK>
-__global__ void __launch_bounds__(32 * kCkWarps)
+__global__ void __launch_bounds__(kCkThreads)
 chunk_scan_kernel(const ChunkArgs a) {
     constexpr int C = kCkC;
     constexpr int KPW = DK / kCkWarps;   // state columns per warp
     constexpr int NJ = KPW / 8;          // 8-column blocks per warp
     constexpr int KS = ck_kstride(DK);
     constexpr int ES = (int)sizeof(TIn);
+    constexpr int VEC = 16 / ES;         // elements per 16-byte piece
+    constexpr int VPR = DK / VEC;        // 16-byte pieces per k / q row
     constexpr int VS = ck_vstride(ES);
+    constexpr int VVR = kCkRows / VEC;   // 16-byte pieces per staged v row
     constexpr int PS = kCkPartStride;
+    constexpr int OS = kCkOutStride;
     extern __shared__ __align__(16) unsigned char smem[];
 
-    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const int64_t n = blockIdx.x / a.row_blocks;
@@ -273,66 +349,71 @@ chunk_scan_kernel(const ChunkArgs a) {
     const int cw = warp * KPW;           // first state column of this warp
     const int64_t nch = a.nchunks;
 
-    const size_t slot_bytes = ck_slot_bytes(DK, ES);
-    auto slotK = [&](int sl) { return reinterpret_cast<TIn *>(smem + sl * slot_bytes); };
+    constexpr size_t kSlot = ck_slot_bytes(DK, ES);
+    constexpr size_t kOffV = align16((size_t)2 * C * KS * ES);
+    constexpr size_t kOffW = kOffV + align16((size_t)C * VS * ES);
+    auto slotK = [&](int sl) { return reinterpret_cast<TIn *>(smem + sl * kSlot); };
     auto slotQ = [&](int sl) { return slotK(sl) + C * KS; };
-    auto slotV = [&](int sl) {
-        return reinterpret_cast<TIn *>(smem + sl * slot_bytes + align16((size_t)2 * C * KS * ES));
-    };
-    auto slotW = [&](int sl) {
-        return reinterpret_cast<float *>(smem + sl * slot_bytes + align16((size_t)2 * C * KS * ES) +
-                                         align16((size_t)C * VS * ES));
-    };
-    float *part = reinterpret_cast<float *>(smem + 3 * slot_bytes);  // [2][warps][16][PS]
+    auto slotV = [&](int sl) { return reinterpret_cast<TIn *>(smem + sl * kSlot + kOffV); };
+    auto slotW = [&](int sl) { return reinterpret_cast<float *>(smem + sl * kSlot + kOffW); };
+    float *part = reinterpret_cast<float *>(smem + 3 * kSlot);         // [2][warps][16][PS]
+    float *otile = part + 2 * kCkWarps * kCkRows * PS;                 // [2][16 steps][OS]
 
     const TIn *qp = static_cast<const TIn *>(a.q);
     const TIn *kp = static_cast<const TIn *>(a.k);
     const TIn *vp = static_cast<const TIn *>(a.v);
+    const bool vec_v = a.vec_v && vlim == kCkRows;
 
-    // ---- issue chunk cc into ring slot cc % 3 (an empty group past the end).
+    // ---- issue chunk cc into ring slot sl (an empty group past the end).
     // Rows of inactive steps are zeroed, never copied: every product of the
     // chunk multiplies them (by zero coefficients, which must not meet NaN).
-    auto issue = [&](int64_t cc) {
+    auto issue = [&](int64_t cc, int sl) {
         if (cc < nch) {
-            const int sl = (int)(cc % 3);
             const int64_t t0 = cc * C;
             const int tcnt = (int)min((int64_t)C, a.T - t0);
             const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
-            if (bits != 0xffffu) {
-                for (int i = tid; i < C * (DK / 4); i += nthr) {
-                    const int tt = i / (DK / 4), x = (i - tt * (DK / 4)) * 4;
-                    if (!((bits >> tt) & 1u)) {
-                        TIn *kr = slotK(sl) + tt * KS + x;
-                        TIn *qr = slotQ(sl) + tt * KS + x;
+            const TIn *ksrc = kp + ((b * a.T + t0) * a.Hk + hk) * DK;
+            const TIn *qsrc = qp + ((b * a.T + t0) * a.Hk + hk) * DK;
+            const int64_t kq_stride = a.Hk * DK;
+            TIn *kd = slotK(sl), *qd = slotQ(sl);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            kr[e] = Elem<TIn>::from_f32(0.f);
-                            qr[e] = Elem<TIn>::from_f32(0.f);
-                        }
-                    }
-                }
-                for (int i = tid; i < C * kCkRows; i += nthr) {
-                    const int tt = i / kCkRows, r = i - tt * kCkRows;
-                    if (!((bits >> tt) & 1u)) slotV(sl)[tt * VS + r] = Elem<TIn>::from_f32(0.f);
+            for (int ii = 0; ii < (C * VPR + kCkThreads - 1) / kCkThreads; ++ii) {
+                const int i = tid + ii * kCkThreads;
+                if ((C * VPR) % kCkThreads != 0 && i >= C * VPR) break;
+                const int tt = i / VPR, x = (i - tt * VPR) * VEC;
+                if ((bits >> tt) & 1u) {
+                    cp_async16(kd + tt * KS + x, ksrc + tt * kq_stride + x);
+                    cp_async16(qd + tt * KS + x, qsrc + tt * kq_stride + x);
+                } else {
+                    *reinterpret_cast<uint4 *>(kd + tt * KS + x) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(qd + tt * KS + x) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            const int64_t kq_off = ((b * a.T + t0) * a.Hk + hk) * DK;
-            async_rows_to<TIn>(slotK(sl), KS, kp + kq_off, a.Hk * DK, tcnt, DK, DK, bits, tid, nthr);
-            async_rows_to<TIn>(slotQ(sl), KS, qp + kq_off, a.Hk * DK, tcnt, DK, DK, bits, tid, nthr);
-            const int64_t v_off = ((b * a.T + t0) * a.Hv + hv) * a.Dv + row0;
-            if (a.vec_v && vlim == kCkRows) {
-                async_rows_to<TIn>(slotV(sl), VS, vp + v_off, a.Hv * a.Dv, tcnt, kCkRows, kCkRows,
-                                   bits, tid, nthr);
-            } else {
-                for (int i = tid; i < tcnt * kCkRows; i += nthr) {
-                    const int tt = i / kCkRows, r = i - tt * kCkRows;
+            const TIn *vsrc = vp + ((b * a.T + t0) * a.Hv + hv) * a.Dv + row0;
+            const int64_t v_stride = a.Hv * a.Dv;
+            TIn *vd = slotV(sl);
+            if (vec_v) {
+                if (tid < C * VVR) {
+                    const int tt = tid / VVR, x = (tid - tt * VVR) * VEC;
                     if ((bits >> tt) & 1u)
-                        slotV(sl)[tt * VS + r] =
-                            r < vlim ? vp[v_off + tt * a.Hv * a.Dv + r] : Elem<TIn>::from_f32(0.f);
+                        cp_async16(vd + tt * VS + x, vsrc + tt * v_stride + x);
+                    else
+                        *reinterpret_cast<uint4 *>(vd + tt * VS + x) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            } else {
+                for (int i = tid; i < C * kCkRows; i += kCkThreads) {
+                    const int tt = i / kCkRows, r = i - tt * kCkRows;
+                    vd[tt * VS + r] = ((bits >> tt) & 1u) && r < vlim ? vsrc[tt * v_stride + r]
+                                                                      : Elem<TIn>::from_f32(0.f);
                 }
             }
             const float *wsrc = a.workspace + (n * nch + cc) * kCkWsFloats;
-            for (int i = tid; i < kCkWsFloats / 4; i += nthr) cp_async16(slotW(sl) + 4 * i, wsrc + 4 * i);
+            float *wd = slotW(sl);
+#pragma unroll
+            for (int ii = 0; ii < (kCkWsFloats / 4 + kCkThreads - 1) / kCkThreads; ++ii) {
+                const int i = tid + ii * kCkThreads;
+                if (i < kCkWsFloats / 4) cp_async16(wd + 4 * i, wsrc + 4 * i);
+            }
         }
         cp_async_commit();
     };
@@ -354,16 +435,19 @@ chunk_scan_kernel(const ChunkArgs a) {
         }
     }
 
-    issue(0);
-    issue(1);
+    issue(0, 0);
+    issue(1, 1);
     cp_async_wait_group<1>();
     __syncthreads();
 
     TIn *yp = static_cast<TIn *>(a.y);
     TIn *dp = static_cast<TIn *>(a.delta_log);
+    const bool out_warp = warp == 0 || (warp == 1 && dp);  // y: warp 0; delta_log: warp 1
+    TIn *const outp = warp == 0 ? yp : dp;
+    float *const mytile = otile + (warp & 1) * C * OS;
 
+    int sl = 0, sl2 = 2;  // ring slots of chunks c and c + 2
     for (int64_t c = 0; c < nch; ++c) {
-        const int sl = (int)(c % 3);
         const int64_t t0 = c * C;
         const int tcnt = (int)min((int64_t)C, a.T - t0);
         const TIn *cK = slotK(sl);
@@ -372,41 +456,41 @@ chunk_scan_kernel(const ChunkArgs a) {
         const float *cW = slotW(sl);
         const float *Wb = cW, *Mq = cW + C * C, *Gam = cW + 2 * C * C, *aC = cW + 2 * C * C + C;
 
-        // ---- P (this warp's columns): [Gam K ; Gam Q] rows as B (n = step),
-        // the state as A (k = column)
-        float P[4][4] = {};  // n-tiles: K steps 0-7, K 8-15, Q 0-7, Q 8-15
-        {
-            const float gam0 = Gam[g], gam1 = Gam[8 + g];
+        // ---- P (this warp's columns, unscaled): [K ; Q] rows as B (n = step),
+        // the state as A (k = column).  Main and small tf32 terms accumulate
+        // in separate registers (two shorter dependency chains).
+        float Pm[4][4] = {}, Ps[4][4] = {};  // n-tiles: K steps 0-7, K 8-15, Q 0-7, Q 8-15
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                uint32_t ah[4], al[4];
-                acc_as_a(S[j], ah, al);
-                const int col = cw + 8 * j + 2 * t;
+        for (int j = 0; j < NJ; ++j) {
+            uint32_t ah[4], al[4];
+            acc_as_a(S[j], ah, al);
+            const int col = cw + 8 * j + 2 * t;
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    const TIn *X = nt < 2 ? cK : cQ;
-                    const int step = 8 * (nt & 1) + g;
-                    const float gm = (nt & 1) ? gam1 : gam0;
-                    const float2 x = ld2f<TIn>(X + step * KS + col);
-                    uint32_t bh0, bl0, bh1, bl1;
-                    split_tf32(gm * x.x, bh0, bl0);
-                    split_tf32(gm * x.y, bh1, bl1);
-                    mma3_tf32(P[nt], ah, al, bh0, bh1, bl0, bl1);
-                }
+            for (int nt = 0; nt < 4; ++nt) {
+                const TIn *X = nt < 2 ? cK : cQ;
+                const float2 x = ld2f<TIn>(X + (8 * (nt & 1) + g) * KS + col);
+                uint32_t bh0, bl0, bh1, bl1;
+                split_tf32(x.x, bh0, bl0);
+                split_tf32(x.y, bh1, bl1);
+                mma_tf32_1688(Ps[nt], al, bh0, bh1);
+                mma_tf32_1688(Ps[nt], ah, bl0, bl1);
+                mma_tf32_1688(Pm[nt], ah, bh0, bh1);
             }
         }
         float *mypart = part + ((c & 1) * kCkWarps + warp) * kCkRows * PS;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-            *reinterpret_cast<float2 *>(mypart + g * PS + 8 * nt + 2 * t) = make_float2(P[nt][0], P[nt][1]);
+            *reinterpret_cast<float2 *>(mypart + g * PS + 8 * nt + 2 * t) =
+                make_float2(Pm[nt][0] + Ps[nt][0], Pm[nt][1] + Ps[nt][1]);
             *reinterpret_cast<float2 *>(mypart + (g + 8) * PS + 8 * nt + 2 * t) =
-                make_float2(P[nt][2], P[nt][3]);
+                make_float2(Pm[nt][2] + Ps[nt][2], Pm[nt][3] + Ps[nt][3]);
         }
         cp_async_wait_group<0>();
         __syncthreads();  // partials of chunk c and the inputs of chunk c+1 are visible
-        issue(c + 2);
+        issue(c + 2, sl2);
 
-        // ---- sum the four partials (P_k for everyone, P_q for the y warp)
+        // ---- sum the four partials and scale by Gam (P_k for every warp, P_q
+        // for the y warp)
         const float *pc = part + (c & 1) * kCkWarps * kCkRows * PS;
         const bool ywarp = warp == 0;
         float Pk[2][4] = {}, Pq[2][4] = {};
@@ -431,6 +515,18 @@ chunk_scan_kernel(const ChunkArgs a) {
                     Pq[nt][3] += w1.y;
                 }
             }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float2 gm = *reinterpret_cast<const float2 *>(Gam + 8 * nt + 2 * t);
+            Pk[nt][0] *= gm.x;
+            Pk[nt][1] *= gm.y;
+            Pk[nt][2] *= gm.x;
+            Pk[nt][3] *= gm.y;
+            Pq[nt][0] *= gm.x;
+            Pq[nt][1] *= gm.y;
+            Pq[nt][2] *= gm.x;
+            Pq[nt][3] *= gm.y;
         }
 
         // ---- R = V^T - P_k;  D = R Wb^T (every warp: D is MMA-2's A operand)
@@ -459,52 +555,62 @@ chunk_scan_kernel(const ChunkArgs a) {
                 }
             }
         }
-        uint32_t dh[2][4], dl[2][4];
-        acc_as_a(D[0], dh[0], dl[0]);
-        acc_as_a(D[1], dh[1], dl[1]);
 
         const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
-        if (ywarp) {
-            // ---- Y = P_q + D Mq^T, stored for active steps of live rows
+        if (out_warp) {
+            if (ywarp) {
+                // ---- Y = P_q + D Mq^T
+                uint32_t dh[2][4], dl[2][4];
+                acc_as_a(D[0], dh[0], dl[0]);
+                acc_as_a(D[1], dh[1], dl[1]);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float2 m = *reinterpret_cast<const float2 *>(Mq + (8 * nt + g) * C + 8 * i + 2 * t);
-                    uint32_t bh0, bl0, bh1, bl1;
-                    split_tf32(m.x, bh0, bl0);
-                    split_tf32(m.y, bh1, bl1);
-                    mma3_tf32(Pq[nt], dh[i], dl[i], bh0, bh1, bl0, bl1);
+                    for (int i = 0; i < 2; ++i) {
+                        const float2 mq = *reinterpret_cast<const float2 *>(Mq + (8 * nt + g) * C + 8 * i + 2 * t);
+                        uint32_t bh0, bl0, bh1, bl1;
+                        split_tf32(mq.x, bh0, bl0);
+                        split_tf32(mq.y, bh1, bl1);
+                        mma3_tf32(Pq[nt], dh[i], dl[i], bh0, bh1, bl0, bl1);
+                    }
                 }
             }
+            // stage the 16 steps x 16 rows tile, then store whole step rows
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int s = 8 * nt + 2 * t + (e & 1), r = g + 8 * (e >> 1);
-                    if (s < tcnt && ((bits >> s) & 1u) && r < vlim)
-                        yp[((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + r] = Elem<TIn>::from_f32(Pq[nt][e]);
-                }
-        } else if (warp == 1 && dp) {
+                for (int e = 0; e < 4; ++e)
+                    mytile[(8 * nt + 2 * t + (e & 1)) * OS + g + 8 * (e >> 1)] = ywarp ? Pq[nt][e] : D[nt][e];
+            __syncwarp();
+            if (a.vec_out && vlim == kCkRows) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int s = 8 * nt + 2 * t + (e & 1), r = g + 8 * (e >> 1);
-                    if (s < tcnt && ((bits >> s) & 1u) && r < vlim)
-                        dp[((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + r] = Elem<TIn>::from_f32(D[nt][e]);
+                for (int h = 0; h < 2; ++h) {
+                    const int s = 8 * h + (lane >> 2), x = 4 * (lane & 3);
+                    if (s < tcnt && ((bits >> s) & 1u))
+                        st4<TIn>(outp + ((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + x,
+                                 *reinterpret_cast<const float4 *>(mytile + s * OS + x));
                 }
+            } else {
+                for (int i = lane; i < C * kCkRows; i += 32) {
+                    const int s = i / kCkRows, r = i - s * kCkRows;
+                    if (s < tcnt && ((bits >> s) & 1u) && r < vlim)
+                        outp[((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + r] =
+                            Elem<TIn>::from_f32(mytile[s * OS + r]);
+                }
+            }
+            __syncwarp();
         }
 
-        // ---- S = Gam_{C-1} S + D (aC K): B = aC-scaled k rows (k = step, n = column)
+        // ---- S = Gam_{C-1} S + (D aC) K: B = raw k rows (k = step, n = column)
         {
-            const float gl = Gam[C - 1];
-            float ac[2][2];
+            uint32_t eh[2][4], el[2][4];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                ac[i][0] = aC[8 * i + 2 * t];
-                ac[i][1] = aC[8 * i + 2 * t + 1];
+                const float2 ac = *reinterpret_cast<const float2 *>(aC + 8 * i + 2 * t);
+                const float de[4] = {D[i][0] * ac.x, D[i][1] * ac.y, D[i][2] * ac.x, D[i][3] * ac.y};
+                acc_as_a(de, eh[i], el[i]);
             }
+            const float gl = Gam[C - 1];
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
 #pragma unroll
@@ -514,12 +620,14 @@ chunk_scan_kernel(const ChunkArgs a) {
                 for (int i = 0; i < 2; ++i) {
                     const int s0 = 8 * i + 2 * t;
                     uint32_t bh0, bl0, bh1, bl1;
-                    split_tf32(ac[i][0] * Elem<TIn>::to_f32(cK[s0 * KS + col]), bh0, bl0);
-                    split_tf32(ac[i][1] * Elem<TIn>::to_f32(cK[(s0 + 1) * KS + col]), bh1, bl1);
-                    mma3_tf32(S[j], dh[i], dl[i], bh0, bh1, bl0, bl1);
+                    split_tf32(Elem<TIn>::to_f32(cK[s0 * KS + col]), bh0, bl0);
+                    split_tf32(Elem<TIn>::to_f32(cK[(s0 + 1) * KS + col]), bh1, bl1);
+                    mma3_tf32(S[j], eh[i], el[i], bh0, bh1, bl0, bl1);
                 }
             }
         }
+        sl = sl == 2 ? 0 : sl + 1;
+        sl2 = sl2 == 2 ? 0 : sl2 + 1;
     }
     cp_async_wait_group<0>();
 
@@ -550,11 +658,10 @@ cudaError_t launch_chunk_dk(const ChunkArgs &a, cudaStream_t st) {
         e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
         if (e != cudaSuccess) return e;
     }
-    const int64_t tiles = a.B * a.Hv;
-    local<<<(unsigned)(tiles * a.nchunks), kCkLocalThreads, lsm, st>>>(a);
+    local<<<(unsigned)(a.B * a.Hk * a.nchunks), kCkLocalThreads, lsm, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    scan<<<(unsigned)(tiles * a.row_blocks), 32 * kCkWarps, ssm, st>>>(a);
+    scan<<<(unsigned)(a.B * a.Hv * a.row_blocks), kCkThreads, ssm, st>>>(a);
     return cudaGetLastError();
 }
 
