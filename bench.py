@@ -48,6 +48,9 @@ KERNEL_SOURCES = os.path.join(ROOT, "linear_attention_recurrence_step_gb300", "c
 
 
 # ---------------------------------------------------------------- accounting
+CHUNK_MIN_T = 256  # bench "auto": calls this long take the chunked prefill
+
+
 def algorithmic_bytes(case, accepted: int, capture: bool = True):
     """Bytes the method must move (each touched once), per launch.
 
@@ -212,7 +215,13 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     lib = gdn.load()
     case = _make_rank_case(args.config, rank, args.batch)
-    uses_repeat = workloads.uses_repeat(args.config)
+    record_path = args.record
+    if record_path == "auto":
+        record_path = "chunk" if case.T >= CHUNK_MIN_T else "step"
+    # the tiled GQA expansion is read in place by the record kernels unless
+    # the materialised repeat is asked for
+    fused_gqa = workloads.uses_repeat(args.config) and args.gqa == "fused"
+    uses_repeat = workloads.uses_repeat(args.config) and not fused_gqa
     dt = case.dtype
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dt]
     code = gdn.DTYPE_CODES[tdt]
@@ -250,6 +259,13 @@ def run_ours(args, rank, world, local_rank):
     rec_args = (q_p, k_p, d_in["v"].data_ptr(), d_in["g"].data_ptr(), d_in["beta"].data_ptr(),
                 d_in["state"].data_ptr(), mask_p, y.data_ptr(), s_rec.data_ptr(), dl.data_ptr(),
                 kl.data_ptr(), gl.data_ptr(), B, T, Hk_rec, Hv, Dk, Dv, code, sp)
+    ws = None
+    if record_path == "chunk":
+        ws = torch.empty(lib.gdn_chunk_prefill_workspace_size(B, T, Hv), dtype=torch.uint8,
+                         device=dev)
+        chunk_args = rec_args[:18] + (1 if fused_gqa else 0, ws.data_ptr(), ws.numel(), code, sp)
+    elif fused_gqa:
+        mapped_args = rec_args[:18] + (1, code, sp)
     rep_args = (dl.data_ptr(), kl.data_ptr(), gl.data_ptr(), d_in["state"].data_ptr(), mask_p,
                 s_rep.data_ptr(), B, T, Hv, Dk, Dv, acc, code, sp)
     eb = workloads.elem_size(dt)
@@ -268,14 +284,19 @@ def run_ours(args, rank, world, local_rank):
             check(lib.gqa_repeat_tiled(*rpt_k), "repeat k")
         if ev is not None:
             ev[0].record(stream)
-        check(lib.gdn_step_record(*rec_args), "record")
+        if record_path == "chunk":
+            check(lib.gdn_chunk_prefill(*chunk_args), "chunk prefill")
+        elif fused_gqa:
+            check(lib.gdn_step_record_mapped(*mapped_args), "record (tiled mapping)")
+        else:
+            check(lib.gdn_step_record(*rec_args), "record")
         if ev is not None:
             ev[1].record(stream)
         check(lib.gdn_state_replay(*rep_args), "replay")
         if ev is not None:
             ev[2].record(stream)
 
-    launches_per_step = 2 + (2 if uses_repeat else 0)
+    launches_per_step = (3 if record_path == "chunk" else 2) + (2 if uses_repeat else 0)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -377,6 +398,10 @@ def run_ours(args, rank, world, local_rank):
             "io_dtype": dt, "state_dtype": "f32", "accepted": acc,
             "mask": workloads.CONFIGS[args.config]["mask"],
             "tape_capture": "delta_log+k_log+g_log",
+            "record_path": ("gdn_chunk_prefill (chunk-local + scan kernels)" if record_path == "chunk"
+                            else "gdn_step_record"),
+            "gqa": ("tiled, read in place" if fused_gqa else
+                    "tiled repeat materialised" if uses_repeat else "block"),
             "l2": f"inputs larger than L2 (state {B * Hv * Dv * Dk * 4 >> 20} MiB per buffer)",
             "parallelism": f"{world} independent batch shard(s), no collective",
         },
@@ -507,6 +532,10 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--record", choices=("auto", "step", "chunk"), default="auto",
+                   help="record entry point: step form, chunked prefill, or by T (auto)")
+    p.add_argument("--gqa", choices=("fused", "repeat"), default="fused",
+                   help="workloads with the tiled GQA expansion: read in place, or materialise")
     p.add_argument("--batch", type=int, default=None,
                    help="override B (smaller cases for profiler captures; not a bench line)")
     args = p.parse_args(argv)

@@ -459,7 +459,9 @@ chunk_scan_kernel(const ChunkArgs a) {
         // ---- P (this warp's columns, unscaled): [K ; Q] rows as B (n = step),
         // the state as A (k = column).  Main and small tf32 terms accumulate
         // in separate registers (two shorter dependency chains).
-        float Pm[4][4] = {}, Ps[4][4] = {};  // n-tiles: K steps 0-7, K 8-15, Q 0-7, Q 8-15
+        // n-tiles: K steps 0-7, K 8-15, Q 0-7, Q 8-15.  The three tf32 terms
+        // accumulate separately: twelve independent chains of NJ products.
+        float Pm[4][4] = {}, Pa[4][4] = {}, Pb[4][4] = {};
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             uint32_t ah[4], al[4];
@@ -472,18 +474,19 @@ chunk_scan_kernel(const ChunkArgs a) {
                 uint32_t bh0, bl0, bh1, bl1;
                 split_tf32(x.x, bh0, bl0);
                 split_tf32(x.y, bh1, bl1);
-                mma_tf32_1688(Ps[nt], al, bh0, bh1);
-                mma_tf32_1688(Ps[nt], ah, bl0, bl1);
+                mma_tf32_1688(Pa[nt], al, bh0, bh1);
+                mma_tf32_1688(Pb[nt], ah, bl0, bl1);
                 mma_tf32_1688(Pm[nt], ah, bh0, bh1);
             }
         }
         float *mypart = part + ((c & 1) * kCkWarps + warp) * kCkRows * PS;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-            *reinterpret_cast<float2 *>(mypart + g * PS + 8 * nt + 2 * t) =
-                make_float2(Pm[nt][0] + Ps[nt][0], Pm[nt][1] + Ps[nt][1]);
-            *reinterpret_cast<float2 *>(mypart + (g + 8) * PS + 8 * nt + 2 * t) =
-                make_float2(Pm[nt][2] + Ps[nt][2], Pm[nt][3] + Ps[nt][3]);
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p[e] = Pm[nt][e] + (Pa[nt][e] + Pb[nt][e]);
+            *reinterpret_cast<float2 *>(mypart + g * PS + 8 * nt + 2 * t) = make_float2(p[0], p[1]);
+            *reinterpret_cast<float2 *>(mypart + (g + 8) * PS + 8 * nt + 2 * t) = make_float2(p[2], p[3]);
         }
         cp_async_wait_group<0>();
         __syncthreads();  // partials of chunk c and the inputs of chunk c+1 are visible
@@ -543,17 +546,24 @@ chunk_scan_kernel(const ChunkArgs a) {
                 r[3] = Elem<TIn>::to_f32(cV[(s0 + 1) * VS + g + 8]) - Pk[i][3];
                 acc_as_a(r, rh[i], rl[i]);
             }
+            float Da[2][4] = {}, Db[2][4] = {};
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+            for (int i = 0; i < 2; ++i) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int nt = 0; nt < 2; ++nt) {
                     const float2 w = *reinterpret_cast<const float2 *>(Wb + (8 * nt + g) * C + 8 * i + 2 * t);
                     uint32_t bh0, bl0, bh1, bl1;
                     split_tf32(w.x, bh0, bl0);
                     split_tf32(w.y, bh1, bl1);
-                    mma3_tf32(D[nt], rh[i], rl[i], bh0, bh1, bl0, bl1);
+                    mma_tf32_1688(Da[nt], rl[i], bh0, bh1);
+                    mma_tf32_1688(Db[nt], rh[i], bl0, bl1);
+                    mma_tf32_1688(D[nt], rh[i], bh0, bh1);
                 }
             }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) D[nt][e] += Da[nt][e] + Db[nt][e];
         }
 
         const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
@@ -611,20 +621,29 @@ chunk_scan_kernel(const ChunkArgs a) {
                 acc_as_a(de, eh[i], el[i]);
             }
             const float gl = Gam[C - 1];
+            float Ua[NJ][4] = {}, Ub[NJ][4] = {};  // small tf32 terms, separate chains
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) S[j][e] *= gl;
-                const int col = cw + 8 * j + g;
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int s0 = 8 * i + 2 * t;
+            for (int i = 0; i < 2; ++i) {
+                const int s0 = 8 * i + 2 * t;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int col = cw + 8 * j + g;
                     uint32_t bh0, bl0, bh1, bl1;
                     split_tf32(Elem<TIn>::to_f32(cK[s0 * KS + col]), bh0, bl0);
                     split_tf32(Elem<TIn>::to_f32(cK[(s0 + 1) * KS + col]), bh1, bl1);
-                    mma3_tf32(S[j], eh[i], el[i], bh0, bh1, bl0, bl1);
+                    mma_tf32_1688(Ua[j], el[i], bh0, bh1);
+                    mma_tf32_1688(Ub[j], eh[i], bl0, bl1);
+                    mma_tf32_1688(S[j], eh[i], bh0, bh1);
                 }
             }
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) S[j][e] += Ua[j][e] + Ub[j][e];
         }
         sl = sl == 2 ? 0 : sl + 1;
         sl2 = sl2 == 2 ? 0 : sl2 + 1;
