@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 3
+#define GDN_ABI_VERSION 4
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st *gdn_stream_t;
@@ -170,6 +170,30 @@ gdn_status gdn_chunk_prefill(const void *q, const void *k, const void *v,
                              int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
                              void *workspace, size_t workspace_bytes,
                              gdn_dtype dtype, gdn_stream_t stream);
+
+/*
+ * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill without a caller workspace.
+ *
+ * The source pages have no counterpart to this entry point: it exists so a
+ * caller that cannot provide device scratch memory can still run the chunked
+ * prefill.  The workspace is a fixed 32 MiB block of device memory that the
+ * library reserves for each device when its code loads (a static device
+ * array; nothing is allocated per call).  Problems whose workspace
+ * (gdn_chunk_prefill_workspace_size) exceeds 32 MiB return
+ * GDN_ERR_UNSUPPORTED before anything is launched.  All calls on one device
+ * share the block, so they must not overlap in time (issue them on one
+ * stream, or use gdn_chunk_prefill with a workspace per stream).  Results
+ * are identical, bit for bit, to gdn_chunk_prefill with the same arguments;
+ * every other argument, rule and error is as documented there.
+ */
+gdn_status gdn_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
+                                     const void *g, const void *beta,
+                                     const float *state_in, const uint32_t *mask,
+                                     void *y, float *state_out, void *delta_log,
+                                     void *k_log, void *g_log,
+                                     int64_t B, int64_t T, int64_t Hk, int64_t Hv,
+                                     int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
+                                     gdn_dtype dtype, gdn_stream_t stream);
 
 /*
  * gdn_state_replay -- rebuild the state after an accepted prefix of the tape

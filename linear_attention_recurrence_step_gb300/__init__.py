@@ -38,7 +38,7 @@ import torch
 from . import _build
 
 __all__ = ["GdnError", "build", "load", "lib_path", "gdn_step_record", "gdn_step_record_mapped",
-           "gdn_chunk_prefill", "gdn_chunk_prefill_workspace_size",
+           "gdn_chunk_prefill", "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc",
            "gdn_state_replay", "gdn_state_replay_per_seq", "gqa_repeat_tiled", "RecordOutputs",
            "STATUS_NAMES", "DTYPE_CODES", "GQA_MAPPINGS"]
 
@@ -47,7 +47,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 GQA_MAPPINGS = {"block": 0, "tiled": 1}
 EXPORTED = ("gdn_step_record", "gdn_step_record_mapped", "gdn_chunk_prefill",
-            "gdn_chunk_prefill_workspace_size", "gdn_state_replay",
+            "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_state_replay",
             "gdn_state_replay_per_seq", "gqa_repeat_tiled", "gdn_status_string",
             "gdn_last_error", "gdn_abi_version")
 
@@ -84,6 +84,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.gdn_chunk_prefill.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int, _P, ctypes.c_size_t,
                                                            ctypes.c_int, _P]
     lib.gdn_chunk_prefill.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_noalloc.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int] * 2 + [_P]
+    lib.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
     lib.gdn_chunk_prefill_workspace_size.argtypes = [_I] * 3
     lib.gdn_chunk_prefill_workspace_size.restype = ctypes.c_size_t
     lib.gdn_state_replay.argtypes = [_P] * 6 + [_I] * 6 + [ctypes.c_int, _P]
@@ -222,7 +224,7 @@ def gdn_chunk_prefill(q, k, v, g, beta, state_in, mask=None, *, y=None, state_ou
     bit-identical to the step form).  ``write_delta=False`` skips the delta
     tape; ``workspace`` (a device tensor of at least
     ``gdn_chunk_prefill_workspace_size(B, T, Hv)`` bytes) is allocated when
-    not given."""
+    not given; ``workspace="static"`` calls gdn_chunk_prefill_noalloc."""
     if gqa not in GQA_MAPPINGS:
         raise ValueError(f"gqa must be one of {sorted(GQA_MAPPINGS)}")
     B, T, Hk, Dk = q.shape
@@ -257,6 +259,15 @@ def gdn_chunk_prefill(q, k, v, g, beta, state_in, mask=None, *, y=None, state_ou
         _need(k_log, "k_log", (B, T, Hv, Dk), dt, dev)
     if g_log is not None:
         _need(g_log, "g_log", (B, T, Hv), dt, dev)
+    if isinstance(workspace, str):
+        if workspace != "static":
+            raise ValueError('workspace must be a device tensor, None or "static"')
+        st = load().gdn_chunk_prefill_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(mask), _ptr(y),
+            _ptr(state_out), _ptr(delta_log), _ptr(k_log), _ptr(g_log), B, T, Hk, Hv, Dk, Dv,
+            GQA_MAPPINGS[gqa], DTYPE_CODES[dt], _stream(dev, stream))
+        _check(st, "gdn_chunk_prefill_noalloc")
+        return RecordOutputs(y, state_out, delta_log, k_log, g_log)
     need = gdn_chunk_prefill_workspace_size(B, T, Hv)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -269,6 +280,12 @@ def gdn_chunk_prefill(q, k, v, g, beta, state_in, mask=None, *, y=None, state_ou
         DTYPE_CODES[dt], _stream(dev, stream))
     _check(st, "gdn_chunk_prefill")
     return RecordOutputs(y, state_out, delta_log, k_log, g_log)
+
+
+def gdn_chunk_prefill_noalloc(q, k, v, g, beta, state_in, mask=None, **kw) -> RecordOutputs:
+    """``gdn_chunk_prefill`` on the library's static 32 MiB scratch (no
+    workspace argument; calls on one device must not overlap in time)."""
+    return gdn_chunk_prefill(q, k, v, g, beta, state_in, mask, workspace="static", **kw)
 
 
 def gdn_state_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted,

@@ -372,6 +372,30 @@ gdn_status gdn_chunk_prefill(const void *q, const void *k, const void *v, const 
                               workspace_bytes, dtype, stream);
 }
 
+gdn_status gdn_chunk_prefill_noalloc(const void *q, const void *k, const void *v, const void *g,
+                                     const void *beta, const float *state_in,
+                                     const uint32_t *mask, void *y, float *state_out,
+                                     void *delta_log, void *k_log, void *g_log, int64_t B,
+                                     int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                                     gdn_gqa_mapping mapping, gdn_dtype dtype,
+                                     gdn_stream_t stream) {
+    static const char *fn = "gdn_chunk_prefill_noalloc";
+    if (B > 0 && T > 0 && Hv > 0) {
+        const int64_t need = gdn::chunk_workspace_bytes(B, T, Hv);
+        if (need < 0 || (uint64_t)need > gdn::kChunkStaticScratchBytes)
+            return fail(GDN_ERR_UNSUPPORTED,
+                        "%s: needs %lld bytes of scratch; the library's static scratch holds %llu "
+                        "(use gdn_chunk_prefill with a caller workspace)",
+                        fn, (long long)need, (unsigned long long)gdn::kChunkStaticScratchBytes);
+    }
+    float *scratch = nullptr;
+    const cudaError_t e = gdn::chunk_static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail(fn, "static scratch address", e);
+    return chunk_prefill_impl(fn, q, k, v, g, beta, state_in, mask, y, state_out, delta_log,
+                              k_log, g_log, B, T, Hk, Hv, Dk, Dv, mapping, scratch,
+                              gdn::kChunkStaticScratchBytes, dtype, stream);
+}
+
 gdn_status gdn_step_record(const void *q, const void *k, const void *v, const void *g,
                            const void *beta, const float *state_in, const uint32_t *mask,
                            void *y, float *state_out, void *delta_log, void *k_log, void *g_log,

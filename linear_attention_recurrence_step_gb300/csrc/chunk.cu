@@ -1,5 +1,7 @@
 // chunk.cu -- launches of the chunked-prefill kernels (chunk.cuh) for every
 // element type and compiled Dk.
+#include <mutex>
+
 #include "chunk.cuh"
 
 namespace gdn {
@@ -11,6 +13,30 @@ cudaError_t launch_chunk(DType dt, int dk, const ChunkArgs &a, cudaStream_t s) {
     case DType::F16: return launch_chunk_type<__half>(dk, a, s);
     }
     return cudaErrorInvalidValue;
+}
+
+// Library-owned scratch for gdn_chunk_prefill_noalloc: one block of device
+// memory per device, reserved when the module loads (never allocated at
+// call time).  Calls that use it must not overlap in time on one device.
+static __device__ __align__(256) float g_chunk_scratch[kChunkStaticScratchBytes / sizeof(float)];
+
+cudaError_t chunk_static_scratch(float **ptr) {
+    constexpr int kMaxDevices = 64;
+    static float *addr[kMaxDevices] = {};
+    static std::mutex lock;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> guard(lock);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_chunk_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<float *>(p);
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
 }
 
 int64_t chunk_workspace_bytes(int64_t B, int64_t T, int64_t Hv) {

@@ -96,5 +96,8 @@ cudaError_t launch_replay(DType dt, int dk, const ReplayArgs &a, const Geometry 
 cudaError_t launch_repeat(const RepeatArgs &a, cudaStream_t s, int sm_count);
 cudaError_t launch_chunk(DType dt, int dk, const ChunkArgs &a, cudaStream_t s);
 int64_t chunk_workspace_bytes(int64_t B, int64_t T, int64_t Hv);  // -1 on overflow
+// The library's static scratch for gdn_chunk_prefill_noalloc (current device).
+constexpr size_t kChunkStaticScratchBytes = (size_t)32 << 20;
+cudaError_t chunk_static_scratch(float **ptr);
 
 }  // namespace gdn

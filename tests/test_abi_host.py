@@ -55,7 +55,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libgdn.so does not export {name}"
-    assert lib.gdn_abi_version() == 3
+    assert lib.gdn_abi_version() == 4
 
 
 def test_library_is_sm103a():
