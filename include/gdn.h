@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 4
+#define GDN_ABI_VERSION 5
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st *gdn_stream_t;
@@ -244,6 +244,45 @@ gdn_status gdn_state_replay_per_seq(const void *delta_log, const void *k_log,
                                     int64_t B, int64_t T, int64_t Hv, int64_t Dk,
                                     int64_t Dv, const int32_t *accepted,
                                     gdn_dtype dtype, gdn_stream_t stream);
+
+/*
+ * gdn_chunk_replay -- gdn_state_replay for long accepted prefixes, as one
+ * tensor-core contraction.
+ *
+ * The replay fold is linear in the state and its updates do not read the
+ * state, so it closes to
+ *     s_out = Gam s_in + sum_t w_t delta_t k_t
+ * over the folded steps t (t < accepted, mask on), with w_t the product of
+ * g_log over the folded steps after t and Gam the product over all of them.
+ * The library forms w and Gam, then runs the sum for every (b, hv) tile as a
+ * (Dv x T) by (T x Dk) product on the tensor cores (tcgen05, tf32 operands
+ * split into high and low parts, float32 accumulation).  Results agree with
+ * gdn_state_replay to float32 rounding, not bit for bit; results are
+ * run-to-run deterministic.
+ *
+ * Arguments, layouts and errors are those of gdn_state_replay, plus:
+ *   accepted_per_seq  [B] int32 (device) or NULL: when given, sequence b folds
+ *                     the steps t < accepted_per_seq[b] (entries < 0 act as 0,
+ *                     > T as T) and `accepted` is only checked to be >= 0
+ *   workspace         caller-owned device memory of at least
+ *                     gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv) bytes,
+ *                     16-byte aligned; one workspace per call in flight
+ * Only state_in, state_out and workspace need 16-byte alignment here.  It
+ * enqueues two or three kernels on `stream` (the decay weights, the
+ * contraction, and a fixed-order sum of partial results when the steps are
+ * split over several CTAs per tile).
+ */
+size_t gdn_chunk_replay_workspace_size(int64_t B, int64_t T, int64_t Hv, int64_t Dk,
+                                       int64_t Dv);
+
+gdn_status gdn_chunk_replay(const void *delta_log, const void *k_log,
+                            const void *g_log, const float *state_in,
+                            const uint32_t *mask, float *state_out,
+                            int64_t B, int64_t T, int64_t Hv, int64_t Dk,
+                            int64_t Dv, int64_t accepted,
+                            const int32_t *accepted_per_seq, void *workspace,
+                            size_t workspace_bytes, gdn_dtype dtype,
+                            gdn_stream_t stream);
 
 /*
  * gqa_repeat_tiled -- tiled GQA broadcast (page: repeat_tiled.rs, "Mapping"):

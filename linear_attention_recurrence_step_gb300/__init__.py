@@ -18,6 +18,9 @@ Entry points (same names as the C ABI):
   16 steps on the tensor cores (float32-accurate; optional tape outputs;
   needs a workspace of ``gdn_chunk_prefill_workspace_size`` bytes, which
   the binding allocates when none is given).
+* ``gdn_chunk_replay`` -- the replay of a long accepted prefix as one
+  tensor-core contraction (tcgen05; float32-accurate; workspace allocated by
+  the binding when none is given).
 * ``gdn_state_replay`` -- re-fold the accepted tape prefix onto a snapshot,
   same page, kernel state_replay.
 * ``gdn_state_replay_per_seq`` -- the same with one accepted count per
@@ -39,6 +42,7 @@ from . import _build
 
 __all__ = ["GdnError", "build", "load", "lib_path", "gdn_step_record", "gdn_step_record_mapped",
            "gdn_chunk_prefill", "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc",
+           "gdn_chunk_replay", "gdn_chunk_replay_workspace_size",
            "gdn_state_replay", "gdn_state_replay_per_seq", "gqa_repeat_tiled", "RecordOutputs",
            "STATUS_NAMES", "DTYPE_CODES", "GQA_MAPPINGS"]
 
@@ -47,7 +51,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 GQA_MAPPINGS = {"block": 0, "tiled": 1}
 EXPORTED = ("gdn_step_record", "gdn_step_record_mapped", "gdn_chunk_prefill",
-            "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_state_replay",
+            "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_chunk_replay",
+            "gdn_chunk_replay_workspace_size", "gdn_state_replay",
             "gdn_state_replay_per_seq", "gqa_repeat_tiled", "gdn_status_string",
             "gdn_last_error", "gdn_abi_version")
 
@@ -86,6 +91,10 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.gdn_chunk_prefill.restype = ctypes.c_int
     lib.gdn_chunk_prefill_noalloc.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int] * 2 + [_P]
     lib.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
+    lib.gdn_chunk_replay.argtypes = [_P] * 6 + [_I] * 6 + [_P, _P, ctypes.c_size_t, ctypes.c_int, _P]
+    lib.gdn_chunk_replay.restype = ctypes.c_int
+    lib.gdn_chunk_replay_workspace_size.argtypes = [_I] * 5
+    lib.gdn_chunk_replay_workspace_size.restype = ctypes.c_size_t
     lib.gdn_chunk_prefill_workspace_size.argtypes = [_I] * 3
     lib.gdn_chunk_prefill_workspace_size.restype = ctypes.c_size_t
     lib.gdn_state_replay.argtypes = [_P] * 6 + [_I] * 6 + [ctypes.c_int, _P]
@@ -319,6 +328,48 @@ def gdn_state_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted,
     else:
         st = load().gdn_state_replay(*ptrs, int(accepted), DTYPE_CODES[dt], _stream(dev, stream))
         _check(st, "gdn_state_replay")
+    return state_out
+
+
+def gdn_chunk_replay_workspace_size(B: int, T: int, Hv: int, Dk: int, Dv: int) -> int:
+    """Bytes of device workspace gdn_chunk_replay needs (0 for invalid sizes)."""
+    return int(load().gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv))
+
+
+def gdn_chunk_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted,
+                     state_out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Replay of the accepted tape prefix as one tensor-core contraction.
+
+    ``accepted`` is an int or an int32 device tensor [B] (per sequence).
+    Float32-accurate, not bit-identical to ``gdn_state_replay``."""
+    B, T, Hv, Dv = delta_log.shape
+    Dk = k_log.shape[3]
+    dt, dev = delta_log.dtype, delta_log.device
+    if dt not in DTYPE_CODES:
+        raise ValueError(f"unsupported dtype {dt}")
+    _need(delta_log, "delta_log", (B, T, Hv, Dv), dt, dev)
+    _need(k_log, "k_log", (B, T, Hv, Dk), dt, dev)
+    _need(g_log, "g_log", (B, T, Hv), dt, dev)
+    _need(state_in, "state_in", (B, Hv, Dv, Dk), torch.float32, dev)
+    if mask is not None:
+        _need(mask, "mask", (B, T), torch.int32 if mask.dtype == torch.int32 else torch.uint32, dev)
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    _need(state_out, "state_out", (B, Hv, Dv, Dk), torch.float32, dev)
+    per_seq = None
+    if isinstance(accepted, torch.Tensor):
+        _need(accepted, "accepted", (B,), torch.int32, dev)
+        per_seq, accepted = accepted, 0
+    need = gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    st = load().gdn_chunk_replay(
+        _ptr(delta_log), _ptr(k_log), _ptr(g_log), _ptr(state_in), _ptr(mask), _ptr(state_out),
+        B, T, Hv, Dk, Dv, int(accepted), _ptr(per_seq), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), DTYPE_CODES[dt], _stream(dev, stream))
+    _check(st, "gdn_chunk_replay")
     return state_out
 
 

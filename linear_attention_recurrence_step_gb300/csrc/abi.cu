@@ -351,9 +351,87 @@ gdn_status chunk_prefill_impl(const char *fn, const void *q, const void *k, cons
     return ok();
 }
 
+gdn_status chunk_replay_impl(const char *fn, const void *delta_log, const void *k_log,
+                             const void *g_log, const float *state_in, const uint32_t *mask,
+                             float *state_out, int64_t B, int64_t T, int64_t Hv, int64_t Dk,
+                             int64_t Dv, int64_t accepted, const int32_t *accepted_per_seq,
+                             void *workspace, size_t workspace_bytes, gdn_dtype dtype,
+                             gdn_stream_t stream) {
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dtype);
+    if (B <= 0 || T <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: B, T, Hv, Dk, Dv must all be > 0 (got %lld %lld %lld %lld %lld)", fn,
+                    (long long)B, (long long)T, (long long)Hv, (long long)Dk, (long long)Dv);
+    if (accepted < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: accepted (%lld) must be >= 0", fn, (long long)accepted);
+    if (!delta_log || !k_log || !g_log || !state_in || !state_out || !workspace)
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: delta_log, k_log, g_log, state_in, state_out, workspace must be non-NULL", fn);
+    if (Dk % 32 != 0 || !gdn::supported_dk(Dk))
+        return fail(GDN_ERR_UNSUPPORTED, "%s: Dk = %lld not supported (32, 64, 128, 192, 256)", fn,
+                    (long long)Dk);
+    const int64_t d_b = nbytes({B, T, Hv, Dv}, eb), kl_b = nbytes({B, T, Hv, Dk}, eb);
+    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), g_b = nbytes({B, T, Hv}, eb);
+    const gdn::ReplayTcPlan plan = gdn::replay_tc_plan(B, T, Hv, Dk, Dv);
+    if (d_b < 0 || kl_b < 0 || s_b < 0 || g_b < 0 || plan.bytes < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: tensor sizes overflow int64", fn);
+    if (workspace_bytes < (uint64_t)plan.bytes)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: workspace too small: need %lld bytes, have %llu", fn,
+                    (long long)plan.bytes, (unsigned long long)workspace_bytes);
+    if (!aligned(state_in, 16) || !aligned(state_out, 16) || !aligned(workspace, 16))
+        return fail(GDN_ERR_MISALIGNED, "%s: state_in, state_out, workspace must be 16-byte aligned", fn);
+    if (!aligned(delta_log, eb) || !aligned(k_log, eb) || !aligned(g_log, eb) || !aligned(mask, 4) ||
+        !aligned(accepted_per_seq, 4))
+        return fail(GDN_ERR_MISALIGNED, "%s: a tensor is not aligned to its element size", fn);
+    if (state_in != state_out && overlap(state_in, s_b, state_out, s_b))
+        return fail(GDN_ERR_INVALID_ARGUMENT,
+                    "%s: state_out overlaps state_in without being the same buffer", fn);
+    const int64_t grid = plan.splits * B * Hv * plan.row_blocks;
+    if (grid > (int64_t)INT32_MAX || B * Hv > (int64_t)INT32_MAX)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large", fn);
+
+    cudaError_t e;
+    const int sms = current_sm_count(&e);
+    if (e != cudaSuccess) return cuda_fail(fn, "device query", e);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    gdn::ReplayTcArgs a{};
+    a.delta_log = delta_log; a.k_log = k_log; a.g_log = g_log;
+    a.state_in = state_in; a.mask = mask; a.state_out = state_out;
+    a.acc_b = accepted_per_seq;
+    a.w = reinterpret_cast<float *>(ws + plan.w_off);
+    a.gam = reinterpret_cast<float *>(ws + plan.gam_off);
+    a.partial = plan.splits > 1 ? reinterpret_cast<float *>(ws + plan.partial_off) : nullptr;
+    a.B = B; a.T = T; a.Hv = Hv; a.Dv = Dv;
+    a.steps = accepted_per_seq ? T : (accepted < T ? accepted : T);
+    a.row_blocks = plan.row_blocks;
+    a.split_steps = plan.split_steps;
+    a.splits = plan.splits;
+    e = gdn::launch_replay_tc(static_cast<gdn::DType>(dtype), (int)Dk, a,
+                              reinterpret_cast<cudaStream_t>(stream), sms);
+    if (e != cudaSuccess) return cuda_fail(fn, "launch", e);
+    return ok();
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t gdn_chunk_replay_workspace_size(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv) {
+    if (B <= 0 || T <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0) return 0;
+    const gdn::ReplayTcPlan plan = gdn::replay_tc_plan(B, T, Hv, Dk, Dv);
+    return plan.bytes < 0 ? 0 : (size_t)plan.bytes;
+}
+
+gdn_status gdn_chunk_replay(const void *delta_log, const void *k_log, const void *g_log,
+                            const float *state_in, const uint32_t *mask, float *state_out,
+                            int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv,
+                            int64_t accepted, const int32_t *accepted_per_seq, void *workspace,
+                            size_t workspace_bytes, gdn_dtype dtype, gdn_stream_t stream) {
+    return chunk_replay_impl("gdn_chunk_replay", delta_log, k_log, g_log, state_in, mask, state_out,
+                             B, T, Hv, Dk, Dv, accepted, accepted_per_seq, workspace,
+                             workspace_bytes, dtype, stream);
+}
 
 size_t gdn_chunk_prefill_workspace_size(int64_t B, int64_t T, int64_t Hv) {
     if (B <= 0 || T <= 0 || Hv <= 0) return 0;

@@ -70,6 +70,23 @@ struct ChunkArgs {
     bool tiled_gqa;      // key head hv % Hk instead of hv / (Hv/Hk)
 };
 
+// Replay as one tensor-core contraction (replay_tc.cuh).
+struct ReplayTcArgs {
+    const void *delta_log, *k_log, *g_log;
+    const float *state_in;
+    const uint32_t *mask;
+    float *state_out;
+    const int32_t *acc_b;  // per-sequence accepted counts or null
+    float *w;              // [B, Hv, T] decay weights (workspace)
+    float *gam;            // [B, Hv] total decay (workspace)
+    float *partial;        // [splits, B, Hv, Dv, Dk] partial sums (workspace) or null
+    int64_t B, T, Hv, Dv;
+    int64_t steps;         // min(accepted, T) (acc_b null) or T
+    int64_t row_blocks;    // ceil(Dv / 128)
+    int64_t split_steps;   // steps per split (multiple of 32)
+    int splits;            // step splits per tile (1: no partial sums)
+};
+
 struct RepeatArgs {
     const void *src;
     void *dst;
@@ -99,5 +116,13 @@ int64_t chunk_workspace_bytes(int64_t B, int64_t T, int64_t Hv);  // -1 on overf
 // The library's static scratch for gdn_chunk_prefill_noalloc (current device).
 constexpr size_t kChunkStaticScratchBytes = (size_t)32 << 20;
 cudaError_t chunk_static_scratch(float **ptr);
+cudaError_t launch_replay_tc(DType dt, int dk, const ReplayTcArgs &a, cudaStream_t s, int sm_count);
+// Split plan and workspace bytes of the tensor-core replay (-1 on overflow).
+struct ReplayTcPlan {
+    int64_t row_blocks, split_steps;
+    int splits;
+    int64_t w_off, gam_off, partial_off, bytes;
+};
+ReplayTcPlan replay_tc_plan(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv);
 
 }  // namespace gdn

@@ -1,0 +1,45 @@
+// replay_tc.cu -- launches of the tensor-core replay (replay_tc.cuh) and its
+// split plan / workspace layout.
+#include "replay_tc.cuh"
+
+namespace gdn {
+
+cudaError_t launch_replay_tc(DType dt, int dk, const ReplayTcArgs &a, cudaStream_t s, int sms) {
+    switch (dt) {
+    case DType::F32: return launch_replay_tc_type<float>(dk, a, s, sms);
+    case DType::BF16: return launch_replay_tc_type<__nv_bfloat16>(dk, a, s, sms);
+    case DType::F16: return launch_replay_tc_type<__half>(dk, a, s, sms);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// Steps are split over CTAs only when the tiles alone give fewer than 128
+// CTAs; the plan depends on the shapes only (not on the device), so the
+// workspace size is a pure function of them.
+ReplayTcPlan replay_tc_plan(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv) {
+    ReplayTcPlan p{};
+    p.bytes = -1;
+    p.row_blocks = (Dv + kTcRows - 1) / kTcRows;
+    int64_t items = 0, nkb = (T + kTcSteps - 1) / kTcSteps;
+    if (__builtin_mul_overflow(B, Hv, &items) || __builtin_mul_overflow(items, p.row_blocks, &items))
+        return p;
+    int64_t splits = items >= 128 ? 1 : std::min<int64_t>(nkb, 128 / items);
+    if (splits < 1) splits = 1;
+    p.split_steps = ((nkb + splits - 1) / splits) * kTcSteps;
+    p.splits = (int)((T + p.split_steps - 1) / p.split_steps);
+    int64_t w = 0, g = 0, part = 0;
+    if (__builtin_mul_overflow(B * Hv, T * 4, &w)) return p;
+    g = B * Hv * 4;
+    if (p.splits > 1) {
+        int64_t per = 0;
+        if (__builtin_mul_overflow(B * Hv, Dv * Dk * 4, &per) || __builtin_mul_overflow(per, (int64_t)p.splits, &part))
+            return p;
+    }
+    p.w_off = 0;
+    p.gam_off = (w + 15) & ~(int64_t)15;
+    p.partial_off = p.gam_off + ((g + 15) & ~(int64_t)15);
+    p.bytes = p.partial_off + part;
+    return p;
+}
+
+}  // namespace gdn

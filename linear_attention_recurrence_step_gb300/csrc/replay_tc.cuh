@@ -1,0 +1,364 @@
+// replay_tc.cuh -- replay of a long accepted prefix as one tensor-core
+// contraction (tcgen05.mma, tf32 operands, accumulator in tensor memory).
+//
+// The replay fold of "metaltile-std gated_delta_replay.rs" (kernel
+// state_replay), s <- g_t s + delta_t k_t over the steps t that are accepted
+// and unmasked, is linear in the state and does not read the state to form
+// its updates, so it closes to
+//     s_out = Gam s_in + sum_t w_t delta_t k_t,
+//     w_t   = prod of g_x over the folded steps x after t,  Gam = prod of all
+// and for every (b, hv) tile the sum is a dense product
+//     S_out = Gam S_in + (delta^T diag(w)) K      (Dv x Dk, contraction over T).
+// replay_weights_kernel forms w and Gam (a suffix product per tile);
+// replay_tc_kernel runs the contraction: the CTA stages 32 steps at a time
+// into shared memory (delta scaled by w as A, k rows as B, both split into
+// tf32 hi + lo terms and stored in the K-major core-matrix layout), one
+// thread issues three tcgen05.mma per 8 steps (a_lo b_hi + a_hi b_lo +
+// a_hi b_hi) into a 128-lane f32 accumulator in tensor memory, and the
+// commit of each stage to an mbarrier frees its buffer for the stage after
+// next.  Long calls split the steps over several CTAs per tile; their
+// partial sums are added in a fixed order by replay_reduce_kernel, so
+// results are run-to-run deterministic.
+//
+// Rows of the tile beyond Dv and steps that are not folded enter as exact
+// zeros (never loaded), so whatever unused tape slots hold cannot reach the
+// state.  Every wait on an mbarrier is bounded (about a second of clock);
+// on expiry the CTA writes NaN to its outputs instead of hanging, releases
+// its tensor memory and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace gdn {
+
+constexpr int kTcRows = 128;       // accumulator lanes = state rows per CTA
+constexpr int kTcThreads = 128;    // four warps: one per 32 tensor-memory lanes
+constexpr int kTcSteps = 32;       // steps staged per pipeline stage
+constexpr int kTcWeightsThreads = 256;
+constexpr long long kTcWaitCycles = 2000000000ll;  // bound on any mbarrier wait
+
+__host__ __device__ constexpr int tc_cols(int dk) {  // tensor-memory columns to allocate
+    return dk <= 32 ? 32 : dk <= 64 ? 64 : dk <= 128 ? 128 : 256;
+}
+// one stage: A hi/lo [128 rows x 32 steps] + B hi/lo [dk x 32 steps], f32
+__host__ __device__ constexpr size_t tc_stage_bytes(int dk) {
+    return (size_t)2 * kTcRows * kTcSteps * 4 + (size_t)2 * dk * kTcSteps * 4;
+}
+__host__ __device__ constexpr size_t replay_tc_smem_bytes(int dk) {
+    return 2 * tc_stage_bytes(dk) + 64;
+}
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ unsigned smem_addr(const void *p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of
+// 8 rows x 16 bytes, `lbo` bytes apart along K and `sbo` bytes apart along
+// M / N (bits 46-48 hold the descriptor version 1).
+__device__ __forceinline__ uint64_t tc_desc(unsigned addr, unsigned lbo, unsigned sbo) {
+    return (uint64_t)((addr >> 4) & 0x3fffu) | ((uint64_t)((lbo >> 4) & 0x3fffu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | (1ull << 46);
+}
+// Instruction descriptor of kind::tf32: f32 accumulator, tf32 A and B, both
+// K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t tc_idesc_tf32(int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcRows >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma_tf32(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void tc_commit(unsigned mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+                 : "memory");
+}
+// Bounded wait for phase `parity` of an mbarrier; false when the bound expired.
+__device__ __forceinline__ bool mbar_wait(unsigned mbar, unsigned parity) {
+    uint32_t done = 0;
+    const long long t0 = clock64();
+    while (!done) {
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(mbar), "r"(parity)
+            : "memory");
+        if (!done && clock64() - t0 > kTcWaitCycles) return false;
+    }
+    return true;
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+        "[%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+}
+// x ~ hi + lo with hi = x rounded to tf32 and lo = x - hi (exact in f32).
+__device__ __forceinline__ void tc_split(float x, float &hi, float &lo) {
+    hi = __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+    lo = x - hi;
+}
+
+// ------------------------------------------------------------ decay weights
+// One CTA per (b, hv): w_t (0 for steps that are not folded) and Gam.
+template <typename TIn>
+__global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const ReplayTcArgs a) {
+    __shared__ float seg[kTcWeightsThreads];
+    __shared__ float suf[kTcWeightsThreads + 1];
+    const int tid = threadIdx.x;
+    const int64_t n = blockIdx.x;
+    const int64_t b = n / a.Hv, hv = n - b * a.Hv;
+    int64_t steps = a.steps;
+    if (a.acc_b) {
+        const int64_t ab = (int64_t)a.acc_b[b];
+        steps = ab < 0 ? 0 : (ab < steps ? ab : steps);
+    }
+    const TIn *glp = static_cast<const TIn *>(a.g_log);
+    const int64_t L = (a.T + kTcWeightsThreads - 1) / kTcWeightsThreads;
+    const int64_t s0 = tid * L, s1 = min(a.T, s0 + L);
+    auto folded = [&](int64_t t) { return t < steps && (!a.mask || a.mask[b * a.T + t] != 0u); };
+    float p = 1.f;
+    for (int64_t t = s0; t < s1; ++t)
+        if (folded(t)) p *= ld_f32(glp + (b * a.T + t) * a.Hv + hv);
+    seg[tid] = p;
+    __syncthreads();
+    if (tid == 0) {  // exclusive suffix products of the segment products
+        float r = 1.f;
+        suf[kTcWeightsThreads] = 1.f;
+        for (int i = kTcWeightsThreads - 1; i >= 0; --i) {
+            suf[i] = r;
+            r *= seg[i];
+        }
+        a.gam[n] = r;
+    }
+    __syncthreads();
+    float run = suf[tid];
+    float *w = a.w + n * a.T;
+    for (int64_t t = s1 - 1; t >= s0; --t) {
+        if (folded(t)) {
+            w[t] = run;
+            run *= ld_f32(glp + (b * a.T + t) * a.Hv + hv);
+        } else {
+            w[t] = 0.f;
+        }
+    }
+}
+
+// ------------------------------------------------------------ the contraction
+template <typename TIn, int DK>
+__global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTcArgs a) {
+    constexpr int KB = kTcSteps;
+    constexpr size_t STAGE = tc_stage_bytes(DK);
+    constexpr unsigned SBO = (KB / 4) * 128;  // bytes between 8-row core-matrix groups
+    constexpr unsigned A_BYTES = kTcRows * KB * 4, B_BYTES = DK * KB * 4;
+    constexpr int NCOL = tc_cols(DK);
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + 2 * STAGE);  // [2]
+    uint32_t *taddr_s = reinterpret_cast<uint32_t *>(smem + 2 * STAGE + 16);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t tiles_rb = a.B * a.Hv * a.row_blocks;
+    const int split = (int)(blockIdx.x / tiles_rb);
+    const int64_t item = blockIdx.x - (int64_t)split * tiles_rb;
+    const int64_t n = item / a.row_blocks, rb = item - n * a.row_blocks;
+    const int64_t b = n / a.Hv, hv = n - b * a.Hv;
+    const int64_t row0 = rb * kTcRows;
+    const int64_t t_begin = (int64_t)split * a.split_steps;
+    const int64_t t_end = min(a.T, t_begin + a.split_steps);
+    const int nstages = t_end > t_begin ? (int)((t_end - t_begin + KB - 1) / KB) : 0;
+    const TIn *dlp = static_cast<const TIn *>(a.delta_log);
+    const TIn *klp = static_cast<const TIn *>(a.k_log);
+    const float *wn = a.w + n * a.T;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(taddr_s)),
+                     "r"(NCOL));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+    }
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&mbar[0])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&mbar[1])));
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    const uint32_t tmem = *taddr_s;
+    const uint32_t idesc = tc_idesc_tf32(DK);
+    bool ok = true;
+    int last_issued = nstages - 1;  // last stage whose MMAs were issued (-1: none)
+
+    // one core matrix (8 rows x 4 steps) per warp instruction: lane -> (row % 8, step % 4)
+    const int cr = lane >> 2, cs = lane & 3;
+    for (int s = 0; s < nstages; ++s) {
+        unsigned char *buf = smem + (s & 1) * STAGE;
+        if (s >= 2) ok = mbar_wait(smem_addr(&mbar[s & 1]), ((s - 2) >> 1) & 1);  // buffer free
+        float *Ah = reinterpret_cast<float *>(buf);
+        float *Al = reinterpret_cast<float *>(buf + A_BYTES);
+        float *Bh = reinterpret_cast<float *>(buf + 2 * A_BYTES);
+        float *Bl = reinterpret_cast<float *>(buf + 2 * A_BYTES + B_BYTES);
+        const int64_t ts = t_begin + (int64_t)s * KB;
+        // A: delta rows scaled by w (row = accumulator lane, k = step)
+        for (int cm = warp; cm < (kTcRows / 8) * (KB / 4); cm += kTcThreads / 32) {
+            const int mi = cm / (KB / 4), ki = cm - mi * (KB / 4);
+            const int r = 8 * mi + cr, tt = 4 * ki + cs;
+            const int64_t t = ts + tt, row = row0 + r;
+            float x = 0.f;
+            if (t < t_end && row < a.Dv) {
+                const float wt = wn[t];
+                if (wt != 0.f) x = wt * ld_f32(dlp + ((b * a.T + t) * a.Hv + hv) * a.Dv + row);
+            }
+            float hi, lo;
+            tc_split(x, hi, lo);
+            const int off = (mi * SBO + ki * 128 + cr * 16 + cs * 4) / 4;
+            Ah[off] = hi;
+            Al[off] = lo;
+        }
+        // B: k rows (n = state column, k = step)
+        for (int cm = warp; cm < (DK / 8) * (KB / 4); cm += kTcThreads / 32) {
+            const int ni = cm / (KB / 4), ki = cm - ni * (KB / 4);
+            const int c = 8 * ni + cr, tt = 4 * ki + cs;
+            const int64_t t = ts + tt;
+            float x = 0.f;
+            if (t < t_end && wn[t] != 0.f) x = ld_f32(klp + ((b * a.T + t) * a.Hv + hv) * DK + c);
+            float hi, lo;
+            tc_split(x, hi, lo);
+            const int off = (ni * SBO + ki * 128 + cr * 16 + cs * 4) / 4;
+            Bh[off] = hi;
+            Bl[off] = lo;
+        }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        ok = __syncthreads_and(ok);  // stage filled (and every wait succeeded, uniformly)
+        if (!ok) {
+            last_issued = s - 1;
+            break;
+        }
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+            const unsigned ah = smem_addr(Ah), al = smem_addr(Al), bh = smem_addr(Bh), bl = smem_addr(Bl);
+#pragma unroll
+            for (int k8 = 0; k8 < KB / 8; ++k8) {
+                const unsigned koff = k8 * 256;  // two core matrices along K per MMA
+                const uint32_t acc0 = (s > 0 || k8 > 0) ? 1u : 0u;
+                tc_mma_tf32(tmem, tc_desc(al + koff, 128, SBO), tc_desc(bh + koff, 128, SBO), idesc, acc0);
+                tc_mma_tf32(tmem, tc_desc(ah + koff, 128, SBO), tc_desc(bl + koff, 128, SBO), idesc, 1u);
+                tc_mma_tf32(tmem, tc_desc(ah + koff, 128, SBO), tc_desc(bh + koff, 128, SBO), idesc, 1u);
+            }
+            tc_commit(smem_addr(&mbar[s & 1]));
+        }
+    }
+    if (last_issued >= 0) {
+        const bool done = mbar_wait(smem_addr(&mbar[last_issued & 1]), (last_issued >> 1) & 1);
+        ok = ok && done;
+    }
+    ok = __syncthreads_and(ok);
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+
+    // epilogue: thread = accumulator lane = state row row0 + 32 warp + lane
+    const int64_t row = row0 + 32 * warp + lane;
+    const bool live = row < a.Dv;
+    const bool direct = a.partial == nullptr;
+    float *dst = direct ? a.state_out + (n * a.Dv + row) * DK
+                        : a.partial + (((int64_t)split * a.B * a.Hv + n) * a.Dv + row) * DK;
+    const float gam = a.gam[n];
+#pragma unroll 1
+    for (int c0 = 0; c0 < DK; c0 += 16) {
+        float v[16];
+        if (ok && last_issued >= 0) {
+            tc_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = ok ? 0.f : __int_as_float(0x7fc00000);
+        }
+        if (live) {
+            if (direct) {
+                const float4 *si = reinterpret_cast<const float4 *>(a.state_in + (n * a.Dv + row) * DK + c0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x = __ldcs(si + q);
+                    v[4 * q + 0] = fmaf(gam, x.x, v[4 * q + 0]);
+                    v[4 * q + 1] = fmaf(gam, x.y, v[4 * q + 1]);
+                    v[4 * q + 2] = fmaf(gam, x.z, v[4 * q + 2]);
+                    v[4 * q + 3] = fmaf(gam, x.w, v[4 * q + 3]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                __stcs(reinterpret_cast<float4 *>(dst + c0) + q,
+                       make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(NCOL));
+}
+
+// S_out = Gam S_in + the partial sums of the step splits, in split order.
+__global__ void __launch_bounds__(256) replay_reduce_kernel(const ReplayTcArgs a, int dk) {
+    const int64_t per_tile = a.Dv * dk / 4;  // float4 per tile
+    const int64_t total = a.B * a.Hv * per_tile;
+    const int64_t plane = a.B * a.Hv * a.Dv * dk / 4;
+    const float4 *si = reinterpret_cast<const float4 *>(a.state_in);
+    const float4 *pp = reinterpret_cast<const float4 *>(a.partial);
+    float4 *so = reinterpret_cast<float4 *>(a.state_out);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float gam = a.gam[i / per_tile];
+        const float4 x = __ldcs(si + i);
+        float4 r = make_float4(gam * x.x, gam * x.y, gam * x.z, gam * x.w);
+        for (int s = 0; s < a.splits; ++s) {
+            const float4 p = __ldcs(pp + s * plane + i);
+            r.x += p.x;
+            r.y += p.y;
+            r.z += p.z;
+            r.w += p.w;
+        }
+        __stcs(so + i, r);
+    }
+}
+
+template <typename TIn, int DK>
+cudaError_t launch_replay_tc_dk(const ReplayTcArgs &a, cudaStream_t st, int sm_count) {
+    auto kern = replay_tc_kernel<TIn, DK>;
+    const size_t sm = replay_tc_smem_bytes(DK);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    replay_weights_kernel<TIn><<<(unsigned)(a.B * a.Hv), kTcWeightsThreads, 0, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(a.splits * a.B * a.Hv * a.row_blocks), kTcThreads, sm, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || a.partial == nullptr) return e;
+    const int64_t total = a.B * a.Hv * a.Dv * DK / 4;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)8 * (sm_count > 0 ? sm_count : 1));
+    replay_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, DK);
+    return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t launch_replay_tc_type(int dk, const ReplayTcArgs &a, cudaStream_t st, int sms) {
+    switch (dk) {
+    case 32: return launch_replay_tc_dk<TIn, 32>(a, st, sms);
+    case 64: return launch_replay_tc_dk<TIn, 64>(a, st, sms);
+    case 128: return launch_replay_tc_dk<TIn, 128>(a, st, sms);
+    case 192: return launch_replay_tc_dk<TIn, 192>(a, st, sms);
+    case 256: return launch_replay_tc_dk<TIn, 256>(a, st, sms);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gdn

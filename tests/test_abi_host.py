@@ -45,7 +45,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("gdn_step_record", "gdn_step_record_mapped", "gdn_chunk_prefill",
-                 "gdn_chunk_prefill_workspace_size", "gdn_state_replay",
+                 "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc",
+                 "gdn_chunk_replay", "gdn_chunk_replay_workspace_size", "gdn_state_replay",
                  "gdn_state_replay_per_seq", "gqa_repeat_tiled",
                  "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
         assert want in names
@@ -55,7 +56,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libgdn.so does not export {name}"
-    assert lib.gdn_abi_version() == 4
+    assert lib.gdn_abi_version() == 5
 
 
 def test_library_is_sm103a():
@@ -135,6 +136,45 @@ def test_chunk_prefill_rejects(lib, name):
     assert msg.startswith("gdn_chunk_prefill")
     if name == "workspace too small":
         assert "need 17408 bytes, have 100" in msg  # 2 x 4 x 1 x 544 x 4
+
+
+def creplay(lib, **kw):
+    ws = lib.gdn_chunk_replay_workspace_size(2, 3, 4, 64, 32)
+    args = dict(delta_log=P(0), k_log=P(1), g_log=P(2), state_in=P(3), mask=None,
+                state_out=P(4), B=2, T=3, Hv=4, Dk=64, Dv=32, accepted=2, per_seq=None,
+                workspace=P(9), workspace_bytes=ws, dtype=F32, stream=None)
+    args.update(kw)
+    return lib.gdn_chunk_replay(*args.values())
+
+
+def test_chunk_replay_workspace_size(lib):
+    # decay weights [B,Hv,T] + totals [B,Hv] (16-byte padded) + partial sums
+    # when the steps are split (fewer than 128 CTAs from the tiles alone)
+    B, T, Hv, Dk, Dv = 1, 4096, 32, 128, 128
+    w, gam = 32 * 4096 * 4, 32 * 4
+    assert lib.gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv) == w + gam + 4 * 32 * 128 * 128 * 4
+    assert lib.gdn_chunk_replay_workspace_size(128, 16, 32, 128, 128) == 128 * 32 * 16 * 4 + 128 * 32 * 4
+    assert lib.gdn_chunk_replay_workspace_size(0, 16, 32, 128, 128) == 0
+
+
+CREPLAY_CASES = {
+    "null workspace": (dict(workspace=None), INVALID),
+    "workspace too small": (dict(workspace_bytes=16), INVALID),
+    "accepted<0": (dict(accepted=-1), INVALID),
+    "null k_log": (dict(k_log=None), INVALID),
+    "Dk=80": (dict(Dk=80), UNSUPPORTED),
+    "dtype": (dict(dtype=4), UNSUPPORTED),
+    "state misaligned": (dict(state_in=P(3) + 4), MISALIGNED),
+    "per_seq misaligned": (dict(per_seq=P(10) + 2), MISALIGNED),
+    "state overlap": (dict(state_out=P(3) + 16), INVALID),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CREPLAY_CASES))
+def test_chunk_replay_rejects(lib, name):
+    kw, want = CREPLAY_CASES[name]
+    assert creplay(lib, **kw) == want
+    assert lib.gdn_last_error().decode().startswith("gdn_chunk_replay")
 
 
 def rep_seq(lib, **kw):

@@ -512,3 +512,75 @@ def test_chunk_prefill_tape_and_in_place(dev):
     on = torch.from_numpy(case.mask.astype(bool)).to(dev)
     assert torch.equal(nodelta["state_out"], got["state_out"])
     assert torch.equal(nodelta["y"][on], got["y"][on])
+
+
+# ------------------------------------------------ replay as one contraction
+CREPLAY_SPECS = [
+    dict(B=2, T=5, Hk=1, Hv=2, Dk=32, Dv=16, dtype="f32", mask="none", accepted=4, seed=901),
+    dict(B=2, T=40, Hk=2, Hv=4, Dk=64, Dv=40, dtype="f32", mask="bernoulli:0.7", accepted=33, seed=902),
+    dict(B=1, T=300, Hk=2, Hv=4, Dk=128, Dv=130, dtype="f32", mask="prefix", accepted="T", seed=903),
+    dict(B=1, T=70, Hk=1, Hv=2, Dk=192, Dv=24, dtype="f32", mask="none", accepted="T", seed=904),
+    dict(B=1, T=90, Hk=1, Hv=1, Dk=256, Dv=128, dtype="f32", mask="bernoulli:0.9", accepted=77, seed=905),
+    dict(B=3, T=64, Hk=2, Hv=4, Dk=128, Dv=64, dtype="bf16", mask="bernoulli:0.8", accepted="T", seed=906),
+    dict(B=2, T=48, Hk=4, Hv=8, Dk=64, Dv=32, dtype="f16", mask="none", accepted=0, seed=907),
+]
+
+
+def _host_tape(case, ref):
+    dt = case.dtype
+    tape = round_to(np.nan_to_num(ref["delta_log"]), dt)
+    kl = round_to(np.nan_to_num(ref["k_log"]), dt)
+    gl = round_to(np.nan_to_num(ref["g_log"]), dt)
+    return tape, kl, gl
+
+
+@pytest.mark.parametrize("spec", CREPLAY_SPECS,
+                         ids=lambda s: f"{s['dtype']}-Dk{s['Dk']}-Dv{s['Dv']}-T{s['T']}-acc{s['accepted']}")
+def test_chunk_replay(dev, spec):
+    """gdn_chunk_replay (tcgen05 contraction) against the oracle's replay of
+    the same host-made tape: split and unsplit step ranges, ragged row
+    blocks (Dv = 130), every Dk, every dtype, masks, accepted 0 / < T / T."""
+    case = workloads.make_case(**spec)
+    ref = oracle.record(*_oracle_inputs(case))
+    tape, kl, gl = _host_tape(case, ref)
+    dt = case.dtype
+    s0 = to_dev(case.state, dev)
+    mask = None if case.mask is None else to_dev(case.mask.astype(np.int32), dev)
+    st = gdn.gdn_chunk_replay(to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev), s0, mask,
+                              accepted=case.accepted)
+    torch.cuda.synchronize()
+    want = oracle.replay(workloads.widen(tape, dt), workloads.widen(kl, dt), workloads.widen(gl, dt),
+                         case.f64("state"), case.mask, accepted=case.accepted)
+    assert_close(to_host_f64(st), want, dt, None, "chunk replay")
+
+
+def test_chunk_replay_long_per_sequence_and_unused_slots(dev):
+    """The long-prefill shape (T = 4096, split over CTAs) with per-sequence
+    counts; NaN in every unused tape slot changes nothing; two runs are
+    bit-identical; in place equals out of place."""
+    case = workloads.make_case(B=2, T=4096, Hk=16, Hv=32, Dk=128, Dv=128, dtype="f32", seed=910,
+                               g_range=(0.95, 1.0), mask="bernoulli:0.9", accepted="T")
+    ref = oracle.record(*_oracle_inputs(case))
+    tape, kl, gl = _host_tape(case, ref)
+    acc = np.array([4096, 2500], dtype=np.int32)
+    s0 = to_dev(case.state, dev)
+    mask = to_dev(case.mask.astype(np.int32), dev)
+    dacc = torch.from_numpy(acc).to(dev)
+    dtape, dkl, dgl = to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev)
+    st = gdn.gdn_chunk_replay(dtape, dkl, dgl, s0, mask, accepted=dacc)
+    want = oracle.replay(tape.astype(np.float64), kl.astype(np.float64), gl.astype(np.float64),
+                         case.f64("state"), case.mask, accepted=acc.astype(np.int64))
+    assert_close(to_host_f64(st), want, "f32", None, "long per-sequence replay")
+    again = gdn.gdn_chunk_replay(dtape, dkl, dgl, s0, mask, accepted=dacc)
+    assert torch.equal(st, again)
+    unused = ~case.mask.astype(bool)
+    unused[1, 2500:] = True
+    dirty = [x.copy() for x in (tape, kl, gl)]
+    for x in dirty:
+        x[unused] = np.nan
+    st_dirty = gdn.gdn_chunk_replay(*(to_dev(x, dev) for x in dirty), s0, mask, accepted=dacc)
+    assert torch.equal(st_dirty, st)
+    s1 = s0.clone()
+    gdn.gdn_chunk_replay(dtape, dkl, dgl, s1, mask, accepted=dacc, state_out=s1)
+    torch.cuda.synchronize()
+    assert torch.equal(s1, st)
