@@ -220,6 +220,9 @@ def run_ours(args, rank, world, local_rank):
         record_path = "chunk" if case.T >= CHUNK_MIN_T else "step"
     # the tiled GQA expansion is read in place by the record kernels unless
     # the materialised repeat is asked for
+    replay_path = args.replay
+    if replay_path == "auto":
+        replay_path = "chunk" if min(case.accepted, case.T) >= CHUNK_MIN_T else "step"
     fused_gqa = workloads.uses_repeat(args.config) and args.gqa == "fused"
     uses_repeat = workloads.uses_repeat(args.config) and not fused_gqa
     dt = case.dtype
@@ -266,6 +269,12 @@ def run_ours(args, rank, world, local_rank):
         chunk_args = rec_args[:18] + (1 if fused_gqa else 0, ws.data_ptr(), ws.numel(), code, sp)
     elif fused_gqa:
         mapped_args = rec_args[:18] + (1, code, sp)
+    if replay_path == "chunk":
+        rws = torch.empty(lib.gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv), dtype=torch.uint8,
+                          device=dev)
+        crep_args = (dl.data_ptr(), kl.data_ptr(), gl.data_ptr(), d_in["state"].data_ptr(), mask_p,
+                     s_rep.data_ptr(), B, T, Hv, Dk, Dv, acc, None, rws.data_ptr(), rws.numel(),
+                     code, sp)
     rep_args = (dl.data_ptr(), kl.data_ptr(), gl.data_ptr(), d_in["state"].data_ptr(), mask_p,
                 s_rep.data_ptr(), B, T, Hv, Dk, Dv, acc, code, sp)
     eb = workloads.elem_size(dt)
@@ -292,11 +301,18 @@ def run_ours(args, rank, world, local_rank):
             check(lib.gdn_step_record(*rec_args), "record")
         if ev is not None:
             ev[1].record(stream)
-        check(lib.gdn_state_replay(*rep_args), "replay")
+        if replay_path == "chunk":
+            check(lib.gdn_chunk_replay(*crep_args), "replay (tensor-core contraction)")
+        else:
+            check(lib.gdn_state_replay(*rep_args), "replay")
         if ev is not None:
             ev[2].record(stream)
 
-    launches_per_step = (3 if record_path == "chunk" else 2) + (2 if uses_repeat else 0)
+    n_replay = 1
+    if replay_path == "chunk":
+        plan_split = rws.numel() > (B * Hv * T * 4 + 15) // 16 * 16 + (B * Hv * 4 + 15) // 16 * 16
+        n_replay = 3 if plan_split else 2
+    launches_per_step = (2 if record_path == "chunk" else 1) + n_replay + (2 if uses_repeat else 0)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -400,6 +416,8 @@ def run_ours(args, rank, world, local_rank):
             "tape_capture": "delta_log+k_log+g_log",
             "record_path": ("gdn_chunk_prefill (chunk-local + scan kernels)" if record_path == "chunk"
                             else "gdn_step_record"),
+            "replay_path": ("gdn_chunk_replay (tcgen05 contraction)" if replay_path == "chunk"
+                            else "gdn_state_replay"),
             "gqa": ("tiled, read in place" if fused_gqa else
                     "tiled repeat materialised" if uses_repeat else "block"),
             "l2": f"inputs larger than L2 (state {B * Hv * Dv * Dk * 4 >> 20} MiB per buffer)",
@@ -534,6 +552,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--record", choices=("auto", "step", "chunk"), default="auto",
                    help="record entry point: step form, chunked prefill, or by T (auto)")
+    p.add_argument("--replay", choices=("auto", "step", "chunk"), default="auto",
+                   help="replay entry point: step form, tensor-core contraction, or by accepted (auto)")
     p.add_argument("--gqa", choices=("fused", "repeat"), default="fused",
                    help="workloads with the tiled GQA expansion: read in place, or materialise")
     p.add_argument("--batch", type=int, default=None,

@@ -34,24 +34,18 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tile.cuh"
 
 namespace gdn {
 
 constexpr int kTcRows = 128;       // accumulator lanes = state rows per CTA
-constexpr int kTcThreads = 128;    // four warps: one per 32 tensor-memory lanes
-constexpr int kTcSteps = 32;       // steps staged per pipeline stage
+constexpr int kTcThreads = 256;    // eight warps: two per 32 tensor-memory lanes
+constexpr int kTcSteps = 16;       // steps staged per pipeline stage
 constexpr int kTcWeightsThreads = 256;
 constexpr long long kTcWaitCycles = 2000000000ll;  // bound on any mbarrier wait
 
 __host__ __device__ constexpr int tc_cols(int dk) {  // tensor-memory columns to allocate
     return dk <= 32 ? 32 : dk <= 64 ? 64 : dk <= 128 ? 128 : 256;
-}
-// one stage: A hi/lo [128 rows x 32 steps] + B hi/lo [dk x 32 steps], f32
-__host__ __device__ constexpr size_t tc_stage_bytes(int dk) {
-    return (size_t)2 * kTcRows * kTcSteps * 4 + (size_t)2 * dk * kTcSteps * 4;
-}
-__host__ __device__ constexpr size_t replay_tc_smem_bytes(int dk) {
-    return 2 * tc_stage_bytes(dk) + 64;
 }
 
 // ------------------------------------------------------------ PTX wrappers
@@ -130,10 +124,15 @@ __global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const
     const TIn *glp = static_cast<const TIn *>(a.g_log);
     const int64_t L = (a.T + kTcWeightsThreads - 1) / kTcWeightsThreads;
     const int64_t s0 = tid * L, s1 = min(a.T, s0 + L);
-    auto folded = [&](int64_t t) { return t < steps && (!a.mask || a.mask[b * a.T + t] != 0u); };
+    // the decay of step t, 1 when t is not folded (loads depend on indices only)
+    auto gfold = [&](int64_t t) {
+        const float gv = ld_f32(glp + (b * a.T + t) * a.Hv + hv);
+        const bool on = t < steps && (!a.mask || a.mask[b * a.T + t] != 0u);
+        return on ? gv : 1.f;
+    };
     float p = 1.f;
-    for (int64_t t = s0; t < s1; ++t)
-        if (folded(t)) p *= ld_f32(glp + (b * a.T + t) * a.Hv + hv);
+#pragma unroll 8
+    for (int64_t t = s0; t < s1; ++t) p *= gfold(t);
     seg[tid] = p;
     __syncthreads();
     if (tid == 0) {  // exclusive suffix products of the segment products
@@ -148,27 +147,53 @@ __global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const
     __syncthreads();
     float run = suf[tid];
     float *w = a.w + n * a.T;
+#pragma unroll 8
     for (int64_t t = s1 - 1; t >= s0; --t) {
-        if (folded(t)) {
-            w[t] = run;
-            run *= ld_f32(glp + (b * a.T + t) * a.Hv + hv);
-        } else {
-            w[t] = 0.f;
-        }
+        const bool on = t < steps && (!a.mask || a.mask[b * a.T + t] != 0u);
+        const float gv = ld_f32(glp + (b * a.T + t) * a.Hv + hv);
+        w[t] = on ? run : 0.f;
+        run = on ? run * gv : run;
     }
 }
 
 // ------------------------------------------------------------ the contraction
-template <typename TIn, int DK>
+// Steps per pipeline stage, and the depth of the raw ring of bulk copies
+// (stages in flight ahead of the fill), within the shared-memory budget.
+__host__ __device__ constexpr int tc_kb(int dk) { return kTcSteps; }
+__host__ __device__ constexpr int tc_raw_depth(int dk) { return dk <= 128 ? 6 : 4; }
+constexpr int kTcRawPitch = kTcRows + 8;  // elements per staged delta row (bank spread)
+__host__ __device__ constexpr int tc_kpitch(int dk) { return dk + 8; }  // per staged k row
+// Raw tape rows of one stage as the bulk copies land them (element type).
+__host__ __device__ constexpr size_t tc_raw_bytes(int dk, int esize) {
+    return align16((size_t)tc_kb(dk) * kTcRawPitch * esize) + align16((size_t)tc_kb(dk) * tc_kpitch(dk) * esize);
+}
+__host__ __device__ constexpr size_t tc_canon_bytes(int dk) {
+    return (size_t)2 * kTcRows * tc_kb(dk) * 4 + (size_t)2 * dk * tc_kb(dk) * 4;
+}
+__host__ __device__ constexpr size_t replay_tc_smem_bytes2(int dk, int esize, bool bulk) {
+    return 2 * tc_canon_bytes(dk) + (bulk ? tc_raw_depth(dk) * tc_raw_bytes(dk, esize) : 0) + 128;
+}
+
+// BULK: the tape rows of each stage arrive by cp.async (16-byte pieces from
+// every thread, RD stages ahead of the fill) into a raw ring in shared
+// memory, and the fill reads them there; the other form loads them from
+// global memory in the fill (any alignment).
+template <typename TIn, int DK, bool BULK>
 __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTcArgs a) {
-    constexpr int KB = kTcSteps;
-    constexpr size_t STAGE = tc_stage_bytes(DK);
-    constexpr unsigned SBO = (KB / 4) * 128;  // bytes between 8-row core-matrix groups
+    constexpr int KB = tc_kb(DK);
+    constexpr int NKQ = KB / 4;               // core matrices along the steps
+    constexpr size_t CANON = tc_canon_bytes(DK);
+    constexpr size_t RAW = tc_raw_bytes(DK, (int)sizeof(TIn));
+    constexpr unsigned SBO = NKQ * 128;       // bytes between 8-row core-matrix groups
     constexpr unsigned A_BYTES = kTcRows * KB * 4, B_BYTES = DK * KB * 4;
     constexpr int NCOL = tc_cols(DK);
+    constexpr int DP = kTcRawPitch, KP = tc_kpitch(DK);
+    constexpr int RD = tc_raw_depth(DK);
     extern __shared__ __align__(1024) unsigned char smem[];
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + 2 * STAGE);  // [2]
-    uint32_t *taddr_s = reinterpret_cast<uint32_t *>(smem + 2 * STAGE + 16);
+    unsigned char *raw0 = smem + 2 * CANON;
+    unsigned char *tail = raw0 + (BULK ? RD * RAW : 0);
+    uint64_t *mbar_mma = reinterpret_cast<uint64_t *>(tail);        // [2]
+    uint32_t *taddr_s = reinterpret_cast<uint32_t *>(tail + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t tiles_rb = a.B * a.Hv * a.row_blocks;
@@ -177,6 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
     const int64_t n = item / a.row_blocks, rb = item - n * a.row_blocks;
     const int64_t b = n / a.Hv, hv = n - b * a.Hv;
     const int64_t row0 = rb * kTcRows;
+    const int rows = (int)min((int64_t)kTcRows, a.Dv - row0);
     const int64_t t_begin = (int64_t)split * a.split_steps;
     const int64_t t_end = min(a.T, t_begin + a.split_steps);
     const int nstages = t_end > t_begin ? (int)((t_end - t_begin + KB - 1) / KB) : 0;
@@ -190,8 +216,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&mbar[0])));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&mbar[1])));
+        for (int i = 0; i < 2; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&mbar_mma[i])));
     }
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
@@ -199,50 +225,95 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
     const uint32_t tmem = *taddr_s;
     const uint32_t idesc = tc_idesc_tf32(DK);
+
+    // cp.async (16-byte pieces, every thread) of stage s's tape rows into raw
+    // slot s % RD, one commit group per stage (empty past the end)
+    constexpr int VEC = 16 / (int)sizeof(TIn);
+    const int dpr = rows / VEC;  // 16-byte pieces per staged delta row
+    auto issue_raw = [&](int s) {
+        if (BULK && s < nstages) {
+            const int64_t ts = t_begin + (int64_t)s * KB;
+            const int cnt = (int)min((int64_t)KB, t_end - ts);
+            TIn *rD = reinterpret_cast<TIn *>(raw0 + (s % RD) * RAW);
+            TIn *rK = reinterpret_cast<TIn *>(raw0 + (s % RD) * RAW + align16((size_t)KB * DP * sizeof(TIn)));
+            for (int i = tid; i < cnt * dpr; i += kTcThreads) {
+                const int tt = i / dpr, x = (i - tt * dpr) * VEC;
+                cp_async16(rD + tt * DP + x, dlp + ((b * a.T + ts + tt) * a.Hv + hv) * a.Dv + row0 + x);
+            }
+#pragma unroll 4
+            for (int i = tid; i < cnt * (DK / VEC); i += kTcThreads) {
+                const int tt = i / (DK / VEC), x = (i - tt * (DK / VEC)) * VEC;
+                cp_async16(rK + tt * KP + x, klp + ((b * a.T + ts + tt) * a.Hv + hv) * DK + x);
+            }
+        }
+        if (BULK) cp_async_commit();
+    };
+    for (int s = 0; s < RD; ++s) issue_raw(s);
+    if (BULK) cp_async_wait_group<RD - 1>();  // stage 0 landed (this thread's pieces)
+    __syncthreads();
+
     bool ok = true;
     int last_issued = nstages - 1;  // last stage whose MMAs were issued (-1: none)
-
     // one core matrix (8 rows x 4 steps) per warp instruction: lane -> (row % 8, step % 4)
     const int cr = lane >> 2, cs = lane & 3;
     for (int s = 0; s < nstages; ++s) {
-        unsigned char *buf = smem + (s & 1) * STAGE;
-        if (s >= 2) ok = mbar_wait(smem_addr(&mbar[s & 1]), ((s - 2) >> 1) & 1);  // buffer free
+        unsigned char *buf = smem + (s & 1) * CANON;
         float *Ah = reinterpret_cast<float *>(buf);
         float *Al = reinterpret_cast<float *>(buf + A_BYTES);
         float *Bh = reinterpret_cast<float *>(buf + 2 * A_BYTES);
         float *Bl = reinterpret_cast<float *>(buf + 2 * A_BYTES + B_BYTES);
         const int64_t ts = t_begin + (int64_t)s * KB;
-        // A: delta rows scaled by w (row = accumulator lane, k = step)
-        for (int cm = warp; cm < (kTcRows / 8) * (KB / 4); cm += kTcThreads / 32) {
-            const int mi = cm / (KB / 4), ki = cm - mi * (KB / 4);
-            const int r = 8 * mi + cr, tt = 4 * ki + cs;
-            const int64_t t = ts + tt, row = row0 + r;
-            float x = 0.f;
-            if (t < t_end && row < a.Dv) {
-                const float wt = wn[t];
-                if (wt != 0.f) x = wt * ld_f32(dlp + ((b * a.T + t) * a.Hv + hv) * a.Dv + row);
-            }
+        // warp w fills core matrices cm = w + 8 j: step quad w % 4, row / column
+        // group 2 j + w / 4 -- one step per lane per stage
+        const int kq = warp & 3, gq = warp >> 2;
+        const int64_t tq0 = ts + 4 * kq + cs;
+        const float w0 = tq0 < t_end ? wn[tq0] : 0.f;
+        if (s >= 2) ok = mbar_wait(smem_addr(&mbar_mma[s & 1]), ((s - 2) >> 1) & 1) && ok;  // buffer free
+        const TIn *rD = reinterpret_cast<const TIn *>(raw0 + (s % RD) * RAW);
+        const TIn *rK = reinterpret_cast<const TIn *>(raw0 + (s % RD) * RAW + align16((size_t)KB * DP * sizeof(TIn)));
+        // Loads first (all independent), then the tf32 splits and the stores:
+        // the staged values and the operand tiles live in the same shared
+        // memory, so interleaving them would order every load after the
+        // previous store.
+        constexpr int NA = kTcRows / 16, NB = DK / 16;  // core matrices per lane
+        float av[NA], bv[NB];
+#pragma unroll
+        for (int j = 0; j < NA; ++j) {  // A: delta rows scaled by w (row = lane of D, k = step)
+            const int r = 8 * (2 * j + gq) + cr;
+            float d = 0.f;
+            if (tq0 < t_end && r < rows)
+                d = BULK ? Elem<TIn>::to_f32(rD[(4 * kq + cs) * DP + r])
+                         : ld_f32(dlp + ((b * a.T + tq0) * a.Hv + hv) * a.Dv + row0 + r);
+            av[j] = d;
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {  // B: k rows (n = state column, k = step)
+            const int c = 8 * (2 * j + gq) + cr;
+            float kv = 0.f;
+            if (tq0 < t_end)
+                kv = BULK ? Elem<TIn>::to_f32(rK[(4 * kq + cs) * KP + c])
+                          : ld_f32(klp + ((b * a.T + tq0) * a.Hv + hv) * DK + c);
+            bv[j] = kv;
+        }
+#pragma unroll
+        for (int j = 0; j < NA; ++j) {
             float hi, lo;
-            tc_split(x, hi, lo);
-            const int off = (mi * SBO + ki * 128 + cr * 16 + cs * 4) / 4;
+            tc_split(w0 != 0.f ? w0 * av[j] : 0.f, hi, lo);
+            const int off = ((2 * j + gq) * SBO + kq * 128 + cr * 16 + cs * 4) / 4;
             Ah[off] = hi;
             Al[off] = lo;
         }
-        // B: k rows (n = state column, k = step)
-        for (int cm = warp; cm < (DK / 8) * (KB / 4); cm += kTcThreads / 32) {
-            const int ni = cm / (KB / 4), ki = cm - ni * (KB / 4);
-            const int c = 8 * ni + cr, tt = 4 * ki + cs;
-            const int64_t t = ts + tt;
-            float x = 0.f;
-            if (t < t_end && wn[t] != 0.f) x = ld_f32(klp + ((b * a.T + t) * a.Hv + hv) * DK + c);
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
             float hi, lo;
-            tc_split(x, hi, lo);
-            const int off = (ni * SBO + ki * 128 + cr * 16 + cs * 4) / 4;
+            tc_split(w0 != 0.f ? bv[j] : 0.f, hi, lo);
+            const int off = ((2 * j + gq) * SBO + kq * 128 + cr * 16 + cs * 4) / 4;
             Bh[off] = hi;
             Bl[off] = lo;
         }
+        if (BULK) cp_async_wait_group<RD - 2>();  // stage s+1 landed (this thread's pieces)
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        ok = __syncthreads_and(ok);  // stage filled (and every wait succeeded, uniformly)
+        ok = __syncthreads_and(ok);  // stage filled, stage s+1 staged (every wait succeeded)
         if (!ok) {
             last_issued = s - 1;
             break;
@@ -258,28 +329,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
                 tc_mma_tf32(tmem, tc_desc(ah + koff, 128, SBO), tc_desc(bl + koff, 128, SBO), idesc, 1u);
                 tc_mma_tf32(tmem, tc_desc(ah + koff, 128, SBO), tc_desc(bh + koff, 128, SBO), idesc, 1u);
             }
-            tc_commit(smem_addr(&mbar[s & 1]));
+            tc_commit(smem_addr(&mbar_mma[s & 1]));
         }
+        issue_raw(s + RD);  // raw slot s % RD was consumed before the barrier
     }
     if (last_issued >= 0) {
-        const bool done = mbar_wait(smem_addr(&mbar[last_issued & 1]), (last_issued >> 1) & 1);
+        const bool done = mbar_wait(smem_addr(&mbar_mma[last_issued & 1]), (last_issued >> 1) & 1);
         ok = ok && done;
     }
+    if (BULK) cp_async_wait_all();  // no copy outlives the CTA
     ok = __syncthreads_and(ok);
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 
-    // epilogue: thread = accumulator lane = state row row0 + 32 warp + lane
-    const int64_t row = row0 + 32 * warp + lane;
+    // epilogue: warp w reads accumulator lanes 32 (w % 4) .. + 31 (its state
+    // rows) and the columns of half w / 4
+    const int64_t row = row0 + 32 * (warp & 3) + lane;
+    const int c_begin = (warp >> 2) * (DK / 2), c_end = c_begin + DK / 2;
     const bool live = row < a.Dv;
     const bool direct = a.partial == nullptr;
     float *dst = direct ? a.state_out + (n * a.Dv + row) * DK
                         : a.partial + (((int64_t)split * a.B * a.Hv + n) * a.Dv + row) * DK;
     const float gam = a.gam[n];
 #pragma unroll 1
-    for (int c0 = 0; c0 < DK; c0 += 16) {
+    for (int c0 = c_begin; c0 < c_end; c0 += 16) {
         float v[16];
         if (ok && last_issued >= 0) {
-            tc_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+            tc_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0, v);
         } else {
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = ok ? 0.f : __int_as_float(0x7fc00000);
@@ -333,8 +408,8 @@ __global__ void __launch_bounds__(256) replay_reduce_kernel(const ReplayTcArgs a
 
 template <typename TIn, int DK>
 cudaError_t launch_replay_tc_dk(const ReplayTcArgs &a, cudaStream_t st, int sm_count) {
-    auto kern = replay_tc_kernel<TIn, DK>;
-    const size_t sm = replay_tc_smem_bytes(DK);
+    auto kern = a.bulk ? replay_tc_kernel<TIn, DK, true> : replay_tc_kernel<TIn, DK, false>;
+    const size_t sm = replay_tc_smem_bytes2(DK, (int)sizeof(TIn), a.bulk);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     replay_weights_kernel<TIn><<<(unsigned)(a.B * a.Hv), kTcWeightsThreads, 0, st>>>(a);
