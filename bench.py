@@ -245,72 +245,86 @@ def run_ours(args, rank, world, local_rank):
         h_in["mask"] = host(case.mask).pin_memory()
     d_in = {n: t.to(dev) for n, t in h_in.items()}
     Hk_rec = Hv if uses_repeat else Hk
-    if uses_repeat:
-        d_in["qx"] = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
-        d_in["kx"] = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
-    y = torch.empty((B, T, Hv, Dv), dtype=tdt, device=dev)
-    dl = torch.empty_like(y)
-    kl = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
-    gl = torch.empty((B, T, Hv), dtype=tdt, device=dev)
-    s_rec = torch.empty_like(d_in["state"])
-    s_rep = torch.empty_like(d_in["state"])
+    eb = workloads.elem_size(dt)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
-    mask_p = d_in["mask"].data_ptr() if "mask" in d_in else None
-    q_p = (d_in["qx"] if uses_repeat else d_in["q"]).data_ptr()
-    k_p = (d_in["kx"] if uses_repeat else d_in["k"]).data_ptr()
-    rec_args = (q_p, k_p, d_in["v"].data_ptr(), d_in["g"].data_ptr(), d_in["beta"].data_ptr(),
-                d_in["state"].data_ptr(), mask_p, y.data_ptr(), s_rec.data_ptr(), dl.data_ptr(),
-                kl.data_ptr(), gl.data_ptr(), B, T, Hk_rec, Hv, Dk, Dv, code, sp)
-    ws = None
-    if record_path == "chunk":
-        ws = torch.empty(lib.gdn_chunk_prefill_workspace_size(B, T, Hv), dtype=torch.uint8,
-                         device=dev)
-        chunk_args = rec_args[:18] + (1 if fused_gqa else 0, ws.data_ptr(), ws.numel(), code, sp)
-    elif fused_gqa:
-        mapped_args = rec_args[:18] + (1, code, sp)
-    if replay_path == "chunk":
-        rws = torch.empty(lib.gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv), dtype=torch.uint8,
-                          device=dev)
-        crep_args = (dl.data_ptr(), kl.data_ptr(), gl.data_ptr(), d_in["state"].data_ptr(), mask_p,
-                     s_rep.data_ptr(), B, T, Hv, Dk, Dv, acc, None, rws.data_ptr(), rws.numel(),
-                     code, sp)
-    rep_args = (dl.data_ptr(), kl.data_ptr(), gl.data_ptr(), d_in["state"].data_ptr(), mask_p,
-                s_rep.data_ptr(), B, T, Hv, Dk, Dv, acc, code, sp)
-    eb = workloads.elem_size(dt)
-    rpt_q = (d_in["q"].data_ptr(), d_in["qx"].data_ptr() if uses_repeat else 0, B * T, Hk, Hv, Dk,
-             code, B * T * Hk * Dk * eb, B * T * Hv * Dk * eb, sp)
-    rpt_k = (d_in["k"].data_ptr(), d_in["kx"].data_ptr() if uses_repeat else 0, B * T, Hk, Hv, Dk,
-             code, B * T * Hk * Dk * eb, B * T * Hv * Dk * eb, sp)
+
+    def alloc_set(inputs=None):
+        """One full set of device buffers for a step: inputs (copied from
+        ``inputs`` or allocated) and every output / workspace."""
+        d = dict(inputs) if inputs is not None else {n: torch.empty_like(t, device=dev)
+                                                     for n, t in h_in.items()}
+        if uses_repeat:
+            d["qx"] = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
+            d["kx"] = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
+        d["y"] = torch.empty((B, T, Hv, Dv), dtype=tdt, device=dev)
+        d["dl"] = torch.empty_like(d["y"])
+        d["kl"] = torch.empty((B, T, Hv, Dk), dtype=tdt, device=dev)
+        d["gl"] = torch.empty((B, T, Hv), dtype=tdt, device=dev)
+        d["s_rec"] = torch.empty_like(d["state"])
+        d["s_rep"] = torch.empty_like(d["state"])
+        if record_path == "chunk":
+            d["ws"] = torch.empty(lib.gdn_chunk_prefill_workspace_size(B, T, Hv), dtype=torch.uint8,
+                                  device=dev)
+        if replay_path == "chunk":
+            d["rws"] = torch.empty(lib.gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv),
+                                   dtype=torch.uint8, device=dev)
+        return d
 
     def check(st, what):
         if st != 0:
             raise RuntimeError(f"{what}: {gdn.STATUS_NAMES.get(st)}: {lib.gdn_last_error().decode()}")
 
-    def step(ev=None):
-        if uses_repeat:
-            check(lib.gqa_repeat_tiled(*rpt_q), "repeat q")
-            check(lib.gqa_repeat_tiled(*rpt_k), "repeat k")
-        if ev is not None:
-            ev[0].record(stream)
+    def make_launcher(d, sp):
+        """The step's launches on buffer set ``d`` and stream ``sp`` (C ABI calls only)."""
+        P = lambda name: d[name].data_ptr()
+        mask_p = P("mask") if "mask" in d else None
+        rec_args = ((P("qx") if uses_repeat else P("q")), (P("kx") if uses_repeat else P("k")), P("v"),
+                    P("g"), P("beta"), P("state"), mask_p, P("y"), P("s_rec"), P("dl"), P("kl"),
+                    P("gl"), B, T, Hk_rec, Hv, Dk, Dv, code, sp)
         if record_path == "chunk":
-            check(lib.gdn_chunk_prefill(*chunk_args), "chunk prefill")
+            rec_call = (lib.gdn_chunk_prefill, rec_args[:18] + (1 if fused_gqa else 0, P("ws"),
+                                                                d["ws"].numel(), code, sp), "chunk prefill")
         elif fused_gqa:
-            check(lib.gdn_step_record_mapped(*mapped_args), "record (tiled mapping)")
+            rec_call = (lib.gdn_step_record_mapped, rec_args[:18] + (1, code, sp), "record (tiled mapping)")
         else:
-            check(lib.gdn_step_record(*rec_args), "record")
-        if ev is not None:
-            ev[1].record(stream)
+            rec_call = (lib.gdn_step_record, rec_args, "record")
         if replay_path == "chunk":
-            check(lib.gdn_chunk_replay(*crep_args), "replay (tensor-core contraction)")
+            rep_call = (lib.gdn_chunk_replay, (P("dl"), P("kl"), P("gl"), P("state"), mask_p, P("s_rep"),
+                                               B, T, Hv, Dk, Dv, acc, None, P("rws"), d["rws"].numel(),
+                                               code, sp), "replay (tensor-core contraction)")
         else:
-            check(lib.gdn_state_replay(*rep_args), "replay")
-        if ev is not None:
-            ev[2].record(stream)
+            rep_call = (lib.gdn_state_replay, (P("dl"), P("kl"), P("gl"), P("state"), mask_p, P("s_rep"),
+                                               B, T, Hv, Dk, Dv, acc, code, sp), "replay")
+        rpts = []
+        if uses_repeat:
+            for src, dst in (("q", "qx"), ("k", "kx")):
+                rpts.append((P(src), P(dst), B * T, Hk, Hv, Dk, code, B * T * Hk * Dk * eb,
+                             B * T * Hv * Dk * eb, sp))
+
+        def launch(ev=None, ev_stream=None):
+            for r in rpts:
+                check(lib.gqa_repeat_tiled(*r), "repeat")
+            if ev is not None:
+                ev[0].record(ev_stream)
+            check(rec_call[0](*rec_call[1]), rec_call[2])
+            if ev is not None:
+                ev[1].record(ev_stream)
+            check(rep_call[0](*rep_call[1]), rep_call[2])
+            if ev is not None:
+                ev[2].record(ev_stream)
+        return launch
+
+    set0 = alloc_set(d_in)
+    y, dl, s_rep = set0["y"], set0["dl"], set0["s_rep"]
+    launch0 = make_launcher(set0, sp)
+
+    def step(ev=None):
+        launch0(ev, stream)
 
     n_replay = 1
     if replay_path == "chunk":
-        plan_split = rws.numel() > (B * Hv * T * 4 + 15) // 16 * 16 + (B * Hv * 4 + 15) // 16 * 16
+        plan_split = set0["rws"].numel() > (B * Hv * T * 4 + 15) // 16 * 16 + (B * Hv * 4 + 15) // 16 * 16
         n_replay = 3 if plan_split else 2
     launches_per_step = (2 if record_path == "chunk" else 1) + n_replay + (2 if uses_repeat else 0)
     for _ in range(args.warmup):
@@ -354,34 +368,59 @@ def run_ours(args, rank, world, local_rank):
         step_bytes += 2 * (B * T * Hk * Dk + B * T * Hv * Dk) * eb
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
-    # ---- end to end through the C ABI with host buffers (pinned): H2D of the
-    # step's inputs, both kernels, D2H of y, the tape and the replayed state.
+    # ---- end to end through the C ABI with host buffers (pinned): every step
+    # copies its inputs host -> device, runs both kernels and copies y, the
+    # delta tape and the replayed state device -> host.  Steps are pipelined
+    # the way a serving loop runs them: two device buffer sets, one stream
+    # each for uploads, kernels and downloads, so the upload of step i+1 and
+    # the download of step i-1 overlap the kernels of step i.
     e2e_steps = max(1, min(args.e2e_steps, K))
-    h_y = torch.empty(y.shape, dtype=tdt).pin_memory()
-    h_dl = torch.empty(dl.shape, dtype=tdt).pin_memory()
-    h_st = torch.empty(s_rep.shape, dtype=torch.float32).pin_memory()
+    h_y = [torch.empty(y.shape, dtype=tdt).pin_memory() for _ in range(2)]
+    h_dl = [torch.empty(dl.shape, dtype=tdt).pin_memory() for _ in range(2)]
+    h_st = [torch.empty(s_rep.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in (h_y, h_dl, h_st))
+    d2h = sum(t.numel() * t.element_size() for t in (h_y[0], h_dl[0], h_st[0]))
+    sets = [set0, alloc_set()]
+    s_up, s_run, s_down = (torch.cuda.Stream(dev) for _ in range(3))
+    launchers = [make_launcher(d, s_run.cuda_stream) for d in sets]
+    up_done = [torch.cuda.Event() for _ in range(2)]
+    run_done = [torch.cuda.Event() for _ in range(2)]
+    down_done = [torch.cuda.Event() for _ in range(2)]
+    for e in down_done:
+        e.record(s_down)
 
-    def e2e_step():
-        for n, t in h_in.items():
-            d_in[n].copy_(t, non_blocking=True)
-        step()
-        h_y.copy_(y, non_blocking=True)
-        h_dl.copy_(dl, non_blocking=True)
-        h_st.copy_(s_rep, non_blocking=True)
+    def e2e_step(i):
+        k = i & 1
+        d = sets[k]
+        s_up.wait_event(down_done[k])   # this set's previous step is fully drained
+        with torch.cuda.stream(s_up):
+            for n, t in h_in.items():
+                d[n].copy_(t, non_blocking=True)
+        up_done[k].record(s_up)
+        s_run.wait_event(up_done[k])
+        launchers[k]()
+        run_done[k].record(s_run)
+        s_down.wait_event(run_done[k])
+        with torch.cuda.stream(s_down):
+            h_y[k].copy_(d["y"], non_blocking=True)
+            h_dl[k].copy_(d["dl"], non_blocking=True)
+            h_st[k].copy_(d["s_rep"], non_blocking=True)
+        down_done[k].record(s_down)
 
-    for _ in range(min(3, args.warmup)):
-        e2e_step()
+    for i in range(min(3, args.warmup)):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_up)
+    s_run.wait_event(e0)
+    s_down.wait_event(e0)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    s_down.wait_event(run_done[(e2e_steps - 1) & 1])
+    e1.record(s_down)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     e2e_value = world * tokens_per_step * e2e_steps / (e2e_ms / 1e3)
@@ -435,7 +474,9 @@ def run_ours(args, rank, world, local_rank):
                        "frac": rep_gbs / peak},
         },
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "mode": "pinned host buffers; uploads, kernels and downloads pipelined on three "
+                        "streams over two device buffer sets"},
         "gpu_launches": launches_per_step * K,
         "clocks": clocks.summary(),
     }
