@@ -431,6 +431,9 @@ CHUNK_SPECS = [
     dict(B=2, T=33, Hk=2, Hv=4, Dk=128, Dv=64, dtype="bf16", mask="bernoulli:0.7", seed=707),
     dict(B=1, T=64, Hk=4, Hv=8, Dk=64, Dv=17, dtype="f16", mask="none", seed=708),
     dict(B=3, T=20, Hk=1, Hv=1, Dk=32, Dv=5, dtype="bf16", mask="all_off", seed=709),
+    # many tiles (B*Hv*ceil(Dv/32) above the SM count): one 16-row m-tile per warp
+    dict(B=8, T=40, Hk=16, Hv=32, Dk=128, Dv=64, dtype="f32", mask="bernoulli:0.8", seed=710),
+    dict(B=6, T=24, Hk=8, Hv=32, Dk=64, Dv=48, dtype="bf16", mask="prefix", seed=711),
 ]
 
 
