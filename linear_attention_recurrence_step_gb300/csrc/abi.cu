@@ -407,7 +407,7 @@ gdn_status chunk_replay_impl(const char *fn, const void *delta_log, const void *
     a.row_blocks = plan.row_blocks;
     a.split_steps = plan.split_steps;
     a.splits = plan.splits;
-    a.bulk = aligned(delta_log, 16) && aligned(k_log, 16) && (Dv * eb) % 16 == 0;
+    a.staged = aligned(delta_log, 16) && aligned(k_log, 16) && (Dv * eb) % 16 == 0;
     e = gdn::launch_replay_tc(static_cast<gdn::DType>(dtype), (int)Dk, a,
                               reinterpret_cast<cudaStream_t>(stream), sms);
     if (e != cudaSuccess) return cuda_fail(fn, "launch", e);

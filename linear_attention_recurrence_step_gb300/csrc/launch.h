@@ -85,7 +85,7 @@ struct ReplayTcArgs {
     int64_t row_blocks;    // ceil(Dv / 128)
     int64_t split_steps;   // steps per split (multiple of 32)
     int splits;            // step splits per tile (1: no partial sums)
-    bool bulk;             // tape rows arrive by bulk copies (16-byte aligned rows)
+    bool staged;           // tape rows are staged with cp.async (16-byte aligned rows)
 };
 
 struct RepeatArgs {

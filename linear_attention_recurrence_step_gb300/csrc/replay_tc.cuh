@@ -10,13 +10,13 @@
 // and for every (b, hv) tile the sum is a dense product
 //     S_out = Gam S_in + (delta^T diag(w)) K      (Dv x Dk, contraction over T).
 // replay_weights_kernel forms w and Gam (a suffix product per tile);
-// replay_tc_kernel runs the contraction: the CTA stages 32 steps at a time
-// into shared memory (delta scaled by w as A, k rows as B, both split into
-// tf32 hi + lo terms and stored in the K-major core-matrix layout), one
-// thread issues three tcgen05.mma per 8 steps (a_lo b_hi + a_hi b_lo +
-// a_hi b_hi) into a 128-lane f32 accumulator in tensor memory, and the
-// commit of each stage to an mbarrier frees its buffer for the stage after
-// next.  Long calls split the steps over several CTAs per tile; their
+// replay_tc_kernel runs the contraction: tape rows arrive by cp.async in a
+// ring several stages ahead, eight warps turn each 16-step stage into
+// operand tiles in shared memory (delta scaled by w as A, k rows as B, both
+// split into tf32 hi + lo terms, K-major core-matrix layout), one thread
+// issues three tcgen05.mma per 8 steps (a_lo b_hi + a_hi b_lo + a_hi b_hi)
+// into a 128-lane f32 accumulator in tensor memory, and the commit of each
+// stage to an mbarrier frees its operand buffer for the stage after next.  Long calls split the steps over several CTAs per tile; their
 // partial sums are added in a fixed order by replay_reduce_kernel, so
 // results are run-to-run deterministic.
 //
@@ -157,28 +157,28 @@ __global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const
 }
 
 // ------------------------------------------------------------ the contraction
-// Steps per pipeline stage, and the depth of the raw ring of bulk copies
+// Steps per pipeline stage, and the depth of the raw ring of cp.async copies
 // (stages in flight ahead of the fill), within the shared-memory budget.
 __host__ __device__ constexpr int tc_kb(int dk) { return kTcSteps; }
 __host__ __device__ constexpr int tc_raw_depth(int dk) { return dk <= 128 ? 6 : 4; }
 constexpr int kTcRawPitch = kTcRows + 8;  // elements per staged delta row (bank spread)
 __host__ __device__ constexpr int tc_kpitch(int dk) { return dk + 8; }  // per staged k row
-// Raw tape rows of one stage as the bulk copies land them (element type).
+// Raw tape rows of one stage as the cp.async copies land them (element type).
 __host__ __device__ constexpr size_t tc_raw_bytes(int dk, int esize) {
     return align16((size_t)tc_kb(dk) * kTcRawPitch * esize) + align16((size_t)tc_kb(dk) * tc_kpitch(dk) * esize);
 }
 __host__ __device__ constexpr size_t tc_canon_bytes(int dk) {
     return (size_t)2 * kTcRows * tc_kb(dk) * 4 + (size_t)2 * dk * tc_kb(dk) * 4;
 }
-__host__ __device__ constexpr size_t replay_tc_smem_bytes2(int dk, int esize, bool bulk) {
-    return 2 * tc_canon_bytes(dk) + (bulk ? tc_raw_depth(dk) * tc_raw_bytes(dk, esize) : 0) + 128;
+__host__ __device__ constexpr size_t replay_tc_smem_bytes2(int dk, int esize, bool staged) {
+    return 2 * tc_canon_bytes(dk) + (staged ? tc_raw_depth(dk) * tc_raw_bytes(dk, esize) : 0) + 128;
 }
 
-// BULK: the tape rows of each stage arrive by cp.async (16-byte pieces from
+// STAGED: the tape rows of each stage arrive by cp.async (16-byte pieces from
 // every thread, RD stages ahead of the fill) into a raw ring in shared
 // memory, and the fill reads them there; the other form loads them from
 // global memory in the fill (any alignment).
-template <typename TIn, int DK, bool BULK>
+template <typename TIn, int DK, bool STAGED>
 __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTcArgs a) {
     constexpr int KB = tc_kb(DK);
     constexpr int NKQ = KB / 4;               // core matrices along the steps
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
     constexpr int RD = tc_raw_depth(DK);
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *raw0 = smem + 2 * CANON;
-    unsigned char *tail = raw0 + (BULK ? RD * RAW : 0);
+    unsigned char *tail = raw0 + (STAGED ? RD * RAW : 0);
     uint64_t *mbar_mma = reinterpret_cast<uint64_t *>(tail);        // [2]
     uint32_t *taddr_s = reinterpret_cast<uint32_t *>(tail + 16);
 
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
     constexpr int VEC = 16 / (int)sizeof(TIn);
     const int dpr = rows / VEC;  // 16-byte pieces per staged delta row
     auto issue_raw = [&](int s) {
-        if (BULK && s < nstages) {
+        if (STAGED && s < nstages) {
             const int64_t ts = t_begin + (int64_t)s * KB;
             const int cnt = (int)min((int64_t)KB, t_end - ts);
             TIn *rD = reinterpret_cast<TIn *>(raw0 + (s % RD) * RAW);
@@ -246,10 +246,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
                 cp_async16(rK + tt * KP + x, klp + ((b * a.T + ts + tt) * a.Hv + hv) * DK + x);
             }
         }
-        if (BULK) cp_async_commit();
+        if (STAGED) cp_async_commit();
     };
     for (int s = 0; s < RD; ++s) issue_raw(s);
-    if (BULK) cp_async_wait_group<RD - 1>();  // stage 0 landed (this thread's pieces)
+    if (STAGED) cp_async_wait_group<RD - 1>();  // stage 0 landed (this thread's pieces)
     __syncthreads();
 
     bool ok = true;
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
             const int r = 8 * (2 * j + gq) + cr;
             float d = 0.f;
             if (tq0 < t_end && r < rows)
-                d = BULK ? Elem<TIn>::to_f32(rD[(4 * kq + cs) * DP + r])
+                d = STAGED ? Elem<TIn>::to_f32(rD[(4 * kq + cs) * DP + r])
                          : ld_f32(dlp + ((b * a.T + tq0) * a.Hv + hv) * a.Dv + row0 + r);
             av[j] = d;
         }
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
             const int c = 8 * (2 * j + gq) + cr;
             float kv = 0.f;
             if (tq0 < t_end)
-                kv = BULK ? Elem<TIn>::to_f32(rK[(4 * kq + cs) * KP + c])
+                kv = STAGED ? Elem<TIn>::to_f32(rK[(4 * kq + cs) * KP + c])
                           : ld_f32(klp + ((b * a.T + tq0) * a.Hv + hv) * DK + c);
             bv[j] = kv;
         }
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
             Bh[off] = hi;
             Bl[off] = lo;
         }
-        if (BULK) cp_async_wait_group<RD - 2>();  // stage s+1 landed (this thread's pieces)
+        if (STAGED) cp_async_wait_group<RD - 2>();  // stage s+1 landed (this thread's pieces)
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         ok = __syncthreads_and(ok);  // stage filled, stage s+1 staged (every wait succeeded)
         if (!ok) {
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) replay_tc_kernel(const ReplayTc
         const bool done = mbar_wait(smem_addr(&mbar_mma[last_issued & 1]), (last_issued >> 1) & 1);
         ok = ok && done;
     }
-    if (BULK) cp_async_wait_all();  // no copy outlives the CTA
+    if (STAGED) cp_async_wait_all();  // no copy outlives the CTA
     ok = __syncthreads_and(ok);
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 
@@ -408,8 +408,8 @@ __global__ void __launch_bounds__(256) replay_reduce_kernel(const ReplayTcArgs a
 
 template <typename TIn, int DK>
 cudaError_t launch_replay_tc_dk(const ReplayTcArgs &a, cudaStream_t st, int sm_count) {
-    auto kern = a.bulk ? replay_tc_kernel<TIn, DK, true> : replay_tc_kernel<TIn, DK, false>;
-    const size_t sm = replay_tc_smem_bytes2(DK, (int)sizeof(TIn), a.bulk);
+    auto kern = a.staged ? replay_tc_kernel<TIn, DK, true> : replay_tc_kernel<TIn, DK, false>;
+    const size_t sm = replay_tc_smem_bytes2(DK, (int)sizeof(TIn), a.staged);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     replay_weights_kernel<TIn><<<(unsigned)(a.B * a.Hv), kTcWeightsThreads, 0, st>>>(a);
