@@ -24,8 +24,9 @@
  *   gdn_last_error() returns a message for the last failure on the calling
  *   host thread.
  * - Floating-point tensors share one element type `dtype` (f32, bf16 or
- *   f16); the recurrent state is always float32.  All arithmetic is float32;
- *   values written in bf16/f16 are rounded to nearest-even.
+ *   f16); the recurrent state is float32 (or `dtype` in the _tstate calls).
+ *   All arithmetic is float32; values written in bf16/f16 are rounded to
+ *   nearest-even.
  *
  * Notation: B batch, T timesteps, Hk key heads, Hv value heads (Hv % Hk == 0,
  * G = Hv / Hk, key head of value head hv is hk = hv / G), Dk key dim, Dv
@@ -45,7 +46,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 5
+#define GDN_ABI_VERSION 6
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st *gdn_stream_t;
@@ -137,6 +138,38 @@ gdn_status gdn_step_record_mapped(const void *q, const void *k, const void *v,
                                   int64_t B, int64_t T, int64_t Hk, int64_t Hv,
                                   int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
                                   gdn_dtype dtype, gdn_stream_t stream);
+
+/*
+ * gdn_step_record_tstate / gdn_state_replay_tstate -- record and replay with
+ * the state stored in the input element type ("state in T", as the page's
+ * kernels keep it) instead of float32.
+ *
+ * state_in / state_out are [B,Hv,Dv,Dk] in `dtype` (16-byte aligned).  The
+ * state is widened exactly on load, every step runs in float32 as in
+ * gdn_step_record, and the final state is rounded to nearest-even once on
+ * store.  With dtype = GDN_DTYPE_F32 these are gdn_step_record_mapped and
+ * gdn_state_replay (or _per_seq) exactly.  Everything else -- arguments,
+ * layouts, mask rule, tape, errors -- is as documented for those calls;
+ * gdn_state_replay_tstate takes the per-sequence counts of
+ * gdn_state_replay_per_seq when accepted_per_seq is non-NULL (then
+ * `accepted` is only checked to be >= 0), else the single count `accepted`.
+ */
+gdn_status gdn_step_record_tstate(const void *q, const void *k, const void *v,
+                                  const void *g, const void *beta,
+                                  const void *state_in, const uint32_t *mask,
+                                  void *y, void *state_out, void *delta_log,
+                                  void *k_log, void *g_log,
+                                  int64_t B, int64_t T, int64_t Hk, int64_t Hv,
+                                  int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
+                                  gdn_dtype dtype, gdn_stream_t stream);
+
+gdn_status gdn_state_replay_tstate(const void *delta_log, const void *k_log,
+                                   const void *g_log, const void *state_in,
+                                   const uint32_t *mask, void *state_out,
+                                   int64_t B, int64_t T, int64_t Hv, int64_t Dk,
+                                   int64_t Dv, int64_t accepted,
+                                   const int32_t *accepted_per_seq,
+                                   gdn_dtype dtype, gdn_stream_t stream);
 
 /*
  * gdn_chunk_prefill -- the record recurrence for long calls, computed in

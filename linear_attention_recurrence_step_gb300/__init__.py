@@ -18,6 +18,9 @@ Entry points (same names as the C ABI):
   16 steps on the tensor cores (float32-accurate; optional tape outputs;
   needs a workspace of ``gdn_chunk_prefill_workspace_size`` bytes, which
   the binding allocates when none is given).
+* ``gdn_step_record_tstate`` / ``gdn_state_replay_tstate`` -- record and
+  replay with the state stored in the input element type (chosen by the
+  binding when ``state_in`` has the inputs' bf16/f16 dtype).
 * ``gdn_chunk_replay`` -- the replay of a long accepted prefix as one
   tensor-core contraction (tcgen05; float32-accurate; workspace allocated by
   the binding when none is given).
@@ -43,6 +46,7 @@ from . import _build
 __all__ = ["GdnError", "build", "load", "lib_path", "gdn_step_record", "gdn_step_record_mapped",
            "gdn_chunk_prefill", "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc",
            "gdn_chunk_replay", "gdn_chunk_replay_workspace_size",
+           "gdn_step_record_tstate", "gdn_state_replay_tstate",
            "gdn_state_replay", "gdn_state_replay_per_seq", "gqa_repeat_tiled", "RecordOutputs",
            "STATUS_NAMES", "DTYPE_CODES", "GQA_MAPPINGS"]
 
@@ -52,7 +56,8 @@ DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 GQA_MAPPINGS = {"block": 0, "tiled": 1}
 EXPORTED = ("gdn_step_record", "gdn_step_record_mapped", "gdn_chunk_prefill",
             "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_chunk_replay",
-            "gdn_chunk_replay_workspace_size", "gdn_state_replay",
+            "gdn_chunk_replay_workspace_size", "gdn_step_record_tstate",
+            "gdn_state_replay_tstate", "gdn_state_replay",
             "gdn_state_replay_per_seq", "gqa_repeat_tiled", "gdn_status_string",
             "gdn_last_error", "gdn_abi_version")
 
@@ -91,6 +96,10 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.gdn_chunk_prefill.restype = ctypes.c_int
     lib.gdn_chunk_prefill_noalloc.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int] * 2 + [_P]
     lib.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
+    lib.gdn_step_record_tstate.argtypes = [_P] * 12 + [_I] * 6 + [ctypes.c_int] * 2 + [_P]
+    lib.gdn_step_record_tstate.restype = ctypes.c_int
+    lib.gdn_state_replay_tstate.argtypes = [_P] * 6 + [_I] * 6 + [_P, ctypes.c_int, _P]
+    lib.gdn_state_replay_tstate.restype = ctypes.c_int
     lib.gdn_chunk_replay.argtypes = [_P] * 6 + [_I] * 6 + [_P, _P, ctypes.c_size_t, ctypes.c_int, _P]
     lib.gdn_chunk_replay.restype = ctypes.c_int
     lib.gdn_chunk_replay_workspace_size.argtypes = [_I] * 5
@@ -179,7 +188,10 @@ def gdn_step_record(q, k, v, g, beta, state_in, mask=None, *, y=None, state_out=
     _need(v, "v", (B, T, Hv, Dv), dt, dev)
     _need(g, "g", (B, T, Hv), dt, dev)
     _need(beta, "beta", (B, T, Hv), dt, dev)
-    _need(state_in, "state_in", (B, Hv, Dv, Dk), torch.float32, dev)
+    # the state is float32, or (state in T) the input element type
+    sdt = state_in.dtype if isinstance(state_in, torch.Tensor) else torch.float32
+    tstate = sdt == dt and dt != torch.float32
+    _need(state_in, "state_in", (B, Hv, Dv, Dk), dt if tstate else torch.float32, dev)
     if mask is not None:
         _need(mask, "mask", (B, T), torch.int32 if mask.dtype == torch.int32 else torch.uint32, dev)
     if y is None:
@@ -194,7 +206,7 @@ def gdn_step_record(q, k, v, g, beta, state_in, mask=None, *, y=None, state_out=
         if g_log is None:
             g_log = torch.empty((B, T, Hv), dtype=dt, device=dev)
     _need(y, "y", (B, T, Hv, Dv), dt, dev)
-    _need(state_out, "state_out", (B, Hv, Dv, Dk), torch.float32, dev)
+    _need(state_out, "state_out", (B, Hv, Dv, Dk), state_in.dtype, dev)
     _need(delta_log, "delta_log", (B, T, Hv, Dv), dt, dev)
     if k_log is not None:
         _need(k_log, "k_log", (B, T, Hv, Dk), dt, dev)
@@ -202,7 +214,11 @@ def gdn_step_record(q, k, v, g, beta, state_in, mask=None, *, y=None, state_out=
         _need(g_log, "g_log", (B, T, Hv), dt, dev)
     ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(mask), _ptr(y),
             _ptr(state_out), _ptr(delta_log), _ptr(k_log), _ptr(g_log), B, T, Hk, Hv, Dk, Dv)
-    if gqa == "block":
+    if tstate:
+        st = load().gdn_step_record_tstate(*ptrs, GQA_MAPPINGS[gqa], DTYPE_CODES[dt],
+                                           _stream(dev, stream))
+        _check(st, "gdn_step_record_tstate")
+    elif gqa == "block":
         st = load().gdn_step_record(*ptrs, DTYPE_CODES[dt], _stream(dev, stream))
         _check(st, "gdn_step_record")
     else:
@@ -312,15 +328,24 @@ def gdn_state_replay(delta_log, k_log, g_log, state_in, mask=None, *, accepted,
     _need(delta_log, "delta_log", (B, T, Hv, Dv), dt, dev)
     _need(k_log, "k_log", (B, T, Hv, Dk), dt, dev)
     _need(g_log, "g_log", (B, T, Hv), dt, dev)
-    _need(state_in, "state_in", (B, Hv, Dv, Dk), torch.float32, dev)
+    sdt = state_in.dtype if isinstance(state_in, torch.Tensor) else torch.float32
+    tstate = sdt == dt and dt != torch.float32
+    _need(state_in, "state_in", (B, Hv, Dv, Dk), dt if tstate else torch.float32, dev)
     if mask is not None:
         _need(mask, "mask", (B, T), torch.int32 if mask.dtype == torch.int32 else torch.uint32, dev)
     if state_out is None:
         state_out = torch.empty_like(state_in)
-    _need(state_out, "state_out", (B, Hv, Dv, Dk), torch.float32, dev)
+    _need(state_out, "state_out", (B, Hv, Dv, Dk), state_in.dtype, dev)
     ptrs = (_ptr(delta_log), _ptr(k_log), _ptr(g_log), _ptr(state_in), _ptr(mask),
             _ptr(state_out), B, T, Hv, Dk, Dv)
-    if isinstance(accepted, torch.Tensor):
+    if tstate:
+        per_seq = accepted if isinstance(accepted, torch.Tensor) else None
+        if per_seq is not None:
+            _need(per_seq, "accepted", (B,), torch.int32, dev)
+        st = load().gdn_state_replay_tstate(*ptrs, 0 if per_seq is not None else int(accepted),
+                                            _ptr(per_seq), DTYPE_CODES[dt], _stream(dev, stream))
+        _check(st, "gdn_state_replay_tstate")
+    elif isinstance(accepted, torch.Tensor):
         _need(accepted, "accepted", (B,), torch.int32, dev)
         st = load().gdn_state_replay_per_seq(*ptrs, _ptr(accepted), DTYPE_CODES[dt],
                                              _stream(dev, stream))

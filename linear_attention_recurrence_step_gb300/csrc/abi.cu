@@ -180,10 +180,10 @@ int gdn_abi_version(void) { return GDN_ABI_VERSION; }
 namespace {
 
 gdn_status record_impl(const char *fn, const void *q, const void *k, const void *v, const void *g,
-                       const void *beta, const float *state_in, const uint32_t *mask, void *y,
-                       float *state_out, void *delta_log, void *k_log, void *g_log, int64_t B,
+                       const void *beta, const void *state_in, const uint32_t *mask, void *y,
+                       void *state_out, void *delta_log, void *k_log, void *g_log, int64_t B,
                        int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
-                       gdn_gqa_mapping mapping, gdn_dtype dtype, gdn_stream_t stream) {
+                       gdn_gqa_mapping mapping, gdn_dtype dtype, bool tstate, gdn_stream_t stream) {
     const int eb = elem_bytes(dtype);
     if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dtype);
     if (mapping != GDN_GQA_BLOCK && mapping != GDN_GQA_TILED)
@@ -202,7 +202,7 @@ gdn_status record_impl(const char *fn, const void *q, const void *k, const void 
         return fail(GDN_ERR_UNSUPPORTED, "%s: Dk = %lld not supported (32, 64, 128, 192, 256)", fn,
                     (long long)Dk);
     const int64_t qk_b = nbytes({B, T, Hk, Dk}, eb), v_b = nbytes({B, T, Hv, Dv}, eb);
-    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), kl_b = nbytes({B, T, Hv, Dk}, eb);
+    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, tstate ? eb : 4), kl_b = nbytes({B, T, Hv, Dk}, eb);
     const int64_t gb_b = nbytes({B, T, Hv}, eb), m_b = nbytes({B, T}, 4);
     if (qk_b < 0 || v_b < 0 || s_b < 0 || kl_b < 0 || gb_b < 0 || m_b < 0)
         return fail(GDN_ERR_INVALID_ARGUMENT, "%s: tensor sizes overflow int64", fn);
@@ -226,7 +226,8 @@ gdn_status record_impl(const char *fn, const void *q, const void *k, const void 
         return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large (B*Hv*row_blocks > 2^31-1)", fn);
     gdn::RecordArgs a{q, k, v, g, beta, state_in, mask, y, state_out, delta_log, k_log, g_log,
                       B, T, Hk, Hv, Dv, geo.rows_cta, geo.row_blocks, geo.tc,
-                      aligned(v, 16) && (Dv * eb) % 16 == 0, mapping == GDN_GQA_TILED};
+                      aligned(v, 16) && (Dv * eb) % 16 == 0, mapping == GDN_GQA_TILED,
+                      tstate && dtype != GDN_DTYPE_F32};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (dtype) {
     case GDN_DTYPE_F32: e = gdn::launch_record_f32((int)Dk, a, geo, s); break;
@@ -238,9 +239,10 @@ gdn_status record_impl(const char *fn, const void *q, const void *k, const void 
 }
 
 gdn_status replay_impl(const char *fn, const void *delta_log, const void *k_log, const void *g_log,
-                       const float *state_in, const uint32_t *mask, float *state_out, int64_t B,
+                       const void *state_in, const uint32_t *mask, void *state_out, int64_t B,
                        int64_t T, int64_t Hv, int64_t Dk, int64_t Dv, int64_t accepted,
-                       const int32_t *accepted_per_seq, gdn_dtype dtype, gdn_stream_t stream) {
+                       const int32_t *accepted_per_seq, gdn_dtype dtype, bool tstate,
+                       gdn_stream_t stream) {
     const int eb = elem_bytes(dtype);
     if (eb == 0) return fail(GDN_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dtype);
     if (B <= 0 || T <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0)
@@ -257,7 +259,7 @@ gdn_status replay_impl(const char *fn, const void *delta_log, const void *k_log,
         return fail(GDN_ERR_UNSUPPORTED, "%s: Dk = %lld not supported (32, 64, 128, 192, 256)", fn,
                     (long long)Dk);
     const int64_t d_b = nbytes({B, T, Hv, Dv}, eb), kl_b = nbytes({B, T, Hv, Dk}, eb);
-    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, 4), g_b = nbytes({B, T, Hv}, eb);
+    const int64_t s_b = nbytes({B, Hv, Dv, Dk}, tstate ? eb : 4), g_b = nbytes({B, T, Hv}, eb);
     const int64_t m_b = nbytes({B, T}, 4);
     if (d_b < 0 || kl_b < 0 || s_b < 0 || g_b < 0 || m_b < 0)
         return fail(GDN_ERR_INVALID_ARGUMENT, "%s: tensor sizes overflow int64", fn);
@@ -281,7 +283,8 @@ gdn_status replay_impl(const char *fn, const void *delta_log, const void *k_log,
         return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large", fn);
     gdn::ReplayArgs a{delta_log, k_log, g_log, state_in, mask, state_out, B, T, Hv, Dv, steps,
                       geo.rows_cta, geo.row_blocks, geo.tc,
-                      aligned(delta_log, 16) && (Dv * eb) % 16 == 0, accepted_per_seq};
+                      aligned(delta_log, 16) && (Dv * eb) % 16 == 0, accepted_per_seq,
+                      tstate && dtype != GDN_DTYPE_F32};
     e = gdn::launch_replay(static_cast<gdn::DType>(dtype), (int)Dk, a, geo,
                            reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(fn, "launch", e);
@@ -481,7 +484,8 @@ gdn_status gdn_step_record(const void *q, const void *k, const void *v, const vo
                            int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
                            gdn_dtype dtype, gdn_stream_t stream) {
     return record_impl("gdn_step_record", q, k, v, g, beta, state_in, mask, y, state_out,
-                       delta_log, k_log, g_log, B, T, Hk, Hv, Dk, Dv, GDN_GQA_BLOCK, dtype, stream);
+                       delta_log, k_log, g_log, B, T, Hk, Hv, Dk, Dv, GDN_GQA_BLOCK, dtype, false,
+                       stream);
 }
 
 gdn_status gdn_step_record_mapped(const void *q, const void *k, const void *v, const void *g,
@@ -491,7 +495,17 @@ gdn_status gdn_step_record_mapped(const void *q, const void *k, const void *v, c
                                   int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
                                   gdn_dtype dtype, gdn_stream_t stream) {
     return record_impl("gdn_step_record_mapped", q, k, v, g, beta, state_in, mask, y, state_out,
-                       delta_log, k_log, g_log, B, T, Hk, Hv, Dk, Dv, mapping, dtype, stream);
+                       delta_log, k_log, g_log, B, T, Hk, Hv, Dk, Dv, mapping, dtype, false, stream);
+}
+
+gdn_status gdn_step_record_tstate(const void *q, const void *k, const void *v, const void *g,
+                                  const void *beta, const void *state_in, const uint32_t *mask,
+                                  void *y, void *state_out, void *delta_log, void *k_log,
+                                  void *g_log, int64_t B, int64_t T, int64_t Hk, int64_t Hv,
+                                  int64_t Dk, int64_t Dv, gdn_gqa_mapping mapping,
+                                  gdn_dtype dtype, gdn_stream_t stream) {
+    return record_impl("gdn_step_record_tstate", q, k, v, g, beta, state_in, mask, y, state_out,
+                       delta_log, k_log, g_log, B, T, Hk, Hv, Dk, Dv, mapping, dtype, true, stream);
 }
 
 gdn_status gdn_state_replay(const void *delta_log, const void *k_log, const void *g_log,
@@ -499,7 +513,7 @@ gdn_status gdn_state_replay(const void *delta_log, const void *k_log, const void
                             int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv,
                             int64_t accepted, gdn_dtype dtype, gdn_stream_t stream) {
     return replay_impl("gdn_state_replay", delta_log, k_log, g_log, state_in, mask, state_out, B,
-                       T, Hv, Dk, Dv, accepted, nullptr, dtype, stream);
+                       T, Hv, Dk, Dv, accepted, nullptr, dtype, false, stream);
 }
 
 gdn_status gdn_state_replay_per_seq(const void *delta_log, const void *k_log, const void *g_log,
@@ -510,7 +524,20 @@ gdn_status gdn_state_replay_per_seq(const void *delta_log, const void *k_log, co
     if (!accepted)
         return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay_per_seq: accepted must be non-NULL");
     return replay_impl("gdn_state_replay_per_seq", delta_log, k_log, g_log, state_in, mask,
-                       state_out, B, T, Hv, Dk, Dv, T, accepted, dtype, stream);
+                       state_out, B, T, Hv, Dk, Dv, T, accepted, dtype, false, stream);
+}
+
+gdn_status gdn_state_replay_tstate(const void *delta_log, const void *k_log, const void *g_log,
+                                   const void *state_in, const uint32_t *mask, void *state_out,
+                                   int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv,
+                                   int64_t accepted, const int32_t *accepted_per_seq,
+                                   gdn_dtype dtype, gdn_stream_t stream) {
+    if (accepted < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_state_replay_tstate: accepted (%lld) must be >= 0",
+                    (long long)accepted);
+    return replay_impl("gdn_state_replay_tstate", delta_log, k_log, g_log, state_in, mask,
+                       state_out, B, T, Hv, Dk, Dv, accepted_per_seq ? T : accepted,
+                       accepted_per_seq, dtype, true, stream);
 }
 
 gdn_status gqa_repeat_tiled(const void *src, void *dst, int64_t seq, int64_t hg, int64_t h,

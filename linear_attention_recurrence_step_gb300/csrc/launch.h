@@ -23,10 +23,10 @@ struct Geometry {
 
 struct RecordArgs {
     const void *q, *k, *v, *g, *beta;
-    const float *state_in;
+    const void *state_in;   // f32, or the input type when tstate
     const uint32_t *mask;
     void *y;
-    float *state_out;
+    void *state_out;
     void *delta_log, *k_log, *g_log;
     int64_t B, T, Hk, Hv, Dv;
     int rows_cta;
@@ -34,13 +34,14 @@ struct RecordArgs {
     int tc;
     bool vec_v;     // v rows can be copied in 16-byte pieces (aligned base, Dv*size % 16 == 0)
     bool tiled_gqa; // key head of value head hv: hv % Hk (tiled) instead of hv / (Hv/Hk) (block)
+    bool tstate;    // the state is stored in the input type (widened on load, rounded on store)
 };
 
 struct ReplayArgs {
     const void *delta_log, *k_log, *g_log;
-    const float *state_in;
+    const void *state_in;   // f32, or the tape type when tstate
     const uint32_t *mask;
-    float *state_out;
+    void *state_out;
     int64_t B, T, Hv, Dv;
     int64_t steps;  // min(accepted, T): steps at or beyond it are never read
     int rows_cta;
@@ -50,6 +51,7 @@ struct ReplayArgs {
     const int32_t *acc_b;  // per-sequence accepted counts [B] (device) or null: then
                            // steps applies to every sequence; else sequence b folds
                            // min(max(acc_b[b], 0), steps) steps
+    bool tstate;           // the state is stored in the tape type
 };
 
 // Chunked prefill (chunk.cuh): record semantics over chunks of 16 steps,

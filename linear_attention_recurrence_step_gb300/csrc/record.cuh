@@ -39,9 +39,12 @@ __host__ __device__ constexpr size_t record_smem_bytes(int dk, int tc, int rows,
            align16((size_t)tc * sizeof(StepScalars)) + align16((size_t)tc * 4) + 16;
 }
 
-template <typename TIn, class Lay>
+// TST: the state is stored in TIn (widened on load, rounded on store);
+// otherwise it is float32.
+template <typename TIn, class Lay, bool TST>
 __global__ void __launch_bounds__(Lay::MAX_THREADS, Lay::MIN_BLOCKS)
 record_kernel(const RecordArgs a) {
+    using TS = typename std::conditional<TST, TIn, float>::type;
     constexpr int DK = Lay::DK;
     constexpr int RT = Lay::RT, NCH = Lay::NCH, L = Lay::L, RW = Lay::RW, REDV = Lay::REDV;
     constexpr bool kF32 = std::is_same<TIn, float>::value;
@@ -129,7 +132,7 @@ record_kernel(const RecordArgs a) {
     // The state slice stays in registers for the whole launch.
     Slice<Lay> s;
     unsigned next_bits = issue(0);
-    load_rows<Lay>(s, a.state_in, n, a.Dv, row0 + lr0, j);
+    load_rows<Lay>(s, static_cast<const TS *>(a.state_in), n, a.Dv, row0 + lr0, j);
     float G_sched = 1.f;  // the scale schedule's running G (kept by the last warp)
 
     const int64_t nchunks = (a.T + TC - 1) / TC;
@@ -256,12 +259,15 @@ record_kernel(const RecordArgs a) {
         }
     }
     const float G = nchunks > 0 ? *s_gfinal : 1.f;
-    store_rows<Lay>(s, G, a.state_out, n, a.Dv, row0 + lr0, j);
+    store_rows<Lay>(s, G, static_cast<TS *>(a.state_out), n, a.Dv, row0 + lr0, j);
 }
 
 template <typename TIn, class Lay>
 cudaError_t launch_record_layout(const RecordArgs &a, const Geometry &geo, cudaStream_t st) {
-    auto kern = record_kernel<TIn, Lay>;
+    auto kern = record_kernel<TIn, Lay, false>;
+    if constexpr (!std::is_same<TIn, float>::value) {
+        if (a.tstate) kern = record_kernel<TIn, Lay, true>;
+    }
     if (geo.smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)geo.smem);

@@ -42,6 +42,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "launch.h"
 #include "record.cuh"
 #include "tile.cuh"
@@ -104,13 +106,32 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, u
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
+// Two consecutive state entries as f32 (exact) and back (nearest-even for bf16).
+__device__ __forceinline__ float2 ld_state2(const float *p) {
+    return __ldcs(reinterpret_cast<const float2 *>(p));
+}
+__device__ __forceinline__ float2 ld_state2(const __nv_bfloat16 *p) {
+    const unsigned raw = __ldcs(reinterpret_cast<const unsigned *>(p));
+    return make_float2(__uint_as_float(raw << 16), __uint_as_float(raw & 0xffff0000u));
+}
+__device__ __forceinline__ void st_state2(float *p, float2 x) {
+    __stcs(reinterpret_cast<float2 *>(p), x);
+}
+__device__ __forceinline__ void st_state2(__nv_bfloat16 *p, float2 x) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+    __stcs(reinterpret_cast<unsigned *>(p), *reinterpret_cast<const unsigned *>(&h));
+}
+
 __device__ __forceinline__ uint32_t lds32(const __nv_bfloat16 *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }
 
-template <int DK>
+// TST: the state is stored in bf16 (widened on load, rounded on store);
+// otherwise it is float32.
+template <int DK, bool TST>
 __global__ void __launch_bounds__(32 * kMmaWarps, kMmaCtasPerSm) record_mma_kernel(const RecordArgs a) {
     using T = __nv_bfloat16;
+    using TS = typename std::conditional<TST, T, float>::type;
     constexpr int NT = DK / 8;   // 8-column blocks of a state row
     constexpr int KT = DK / 16;  // k16 tiles along Dk
     constexpr int KS = mma_kstride(DK);
@@ -209,12 +230,13 @@ __global__ void __launch_bounds__(32 * kMmaWarps, kMmaCtasPerSm) record_mma_kern
     unsigned next_bits = issue(0);
     float st[NT][4];
     {
-        const float2 *s0 = reinterpret_cast<const float2 *>(a.state_in + (n * a.Dv + row0 + lr[0]) * DK);
-        const float2 *s1 = reinterpret_cast<const float2 *>(a.state_in + (n * a.Dv + row0 + lr[1]) * DK);
+        const TS *sin = static_cast<const TS *>(a.state_in);
+        const TS *s0 = sin + (n * a.Dv + row0 + lr[0]) * DK;
+        const TS *s1 = sin + (n * a.Dv + row0 + lr[1]) * DK;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-            const float2 x = live0 ? __ldcs(s0 + 4 * j + t) : make_float2(0.f, 0.f);
-            const float2 y = live1 ? __ldcs(s1 + 4 * j + t) : make_float2(0.f, 0.f);
+            const float2 x = live0 ? ld_state2(s0 + 8 * j + 2 * t) : make_float2(0.f, 0.f);
+            const float2 y = live1 ? ld_state2(s1 + 8 * j + 2 * t) : make_float2(0.f, 0.f);
             st[j][0] = x.x;
             st[j][1] = x.y;
             st[j][2] = y.x;
@@ -529,18 +551,19 @@ __global__ void __launch_bounds__(32 * kMmaWarps, kMmaCtasPerSm) record_mma_kern
 
     // ---- s = G s^, streaming stores
     const float G = nchunks > 0 ? *s_gfinal : 1.f;
-    float2 *o0 = reinterpret_cast<float2 *>(a.state_out + (n * a.Dv + row0 + lr[0]) * DK);
-    float2 *o1 = reinterpret_cast<float2 *>(a.state_out + (n * a.Dv + row0 + lr[1]) * DK);
+    TS *sout = static_cast<TS *>(a.state_out);
+    TS *o0 = sout + (n * a.Dv + row0 + lr[0]) * DK;
+    TS *o1 = sout + (n * a.Dv + row0 + lr[1]) * DK;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-        if (live0) __stcs(o0 + 4 * j + t, make_float2(st[j][0] * G, st[j][1] * G));
-        if (live1) __stcs(o1 + 4 * j + t, make_float2(st[j][2] * G, st[j][3] * G));
+        if (live0) st_state2(o0 + 8 * j + 2 * t, make_float2(st[j][0] * G, st[j][1] * G));
+        if (live1) st_state2(o1 + 8 * j + 2 * t, make_float2(st[j][2] * G, st[j][3] * G));
     }
 }
 
 template <int DK>
 cudaError_t launch_record_mma(const RecordArgs &a, const Geometry &geo, cudaStream_t st) {
-    auto kern = record_mma_kernel<DK>;
+    auto kern = a.tstate ? record_mma_kernel<DK, true> : record_mma_kernel<DK, false>;
     if (geo.smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)geo.smem);

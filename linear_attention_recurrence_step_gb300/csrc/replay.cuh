@@ -34,9 +34,12 @@ __host__ __device__ constexpr size_t replay_smem_bytes(int dk, int tc, int rows,
            align16((size_t)tc * sizeof(StepScalars)) + align16((size_t)tc * 4) + 16;
 }
 
-template <typename TIn, class Lay>
+// TST: the state is stored in TIn (widened on load, rounded on store);
+// otherwise it is float32.
+template <typename TIn, class Lay, bool TST>
 __global__ void __launch_bounds__(Lay::MAX_THREADS, Lay::MIN_BLOCKS)
 replay_kernel(const ReplayArgs a) {
+    using TS = typename std::conditional<TST, TIn, float>::type;
     constexpr int DK = Lay::DK;
     constexpr int RT = Lay::RT, NCH = Lay::NCH, L = Lay::L, RW = Lay::RW;
     constexpr bool kF32 = std::is_same<TIn, float>::value;
@@ -108,7 +111,7 @@ replay_kernel(const ReplayArgs a) {
     Slice<Lay> s;
     const int64_t nchunks = (steps + TC - 1) / TC;
     unsigned next_bits = nchunks > 0 ? issue(0) : 0u;
-    load_rows<Lay>(s, a.state_in, n, a.Dv, row0 + lr0, j);
+    load_rows<Lay>(s, static_cast<const TS *>(a.state_in), n, a.Dv, row0 + lr0, j);
     float G_sched = 1.f;
 
     for (int64_t c = 0; c < nchunks; ++c) {
@@ -168,12 +171,15 @@ replay_kernel(const ReplayArgs a) {
         }
     }
     const float G = nchunks > 0 ? *s_gfinal : 1.f;
-    store_rows<Lay>(s, G, a.state_out, n, a.Dv, row0 + lr0, j);
+    store_rows<Lay>(s, G, static_cast<TS *>(a.state_out), n, a.Dv, row0 + lr0, j);
 }
 
 template <typename TIn, class Lay>
 cudaError_t launch_replay_layout(const ReplayArgs &a, const Geometry &geo, cudaStream_t st) {
-    auto kern = replay_kernel<TIn, Lay>;
+    auto kern = replay_kernel<TIn, Lay, false>;
+    if constexpr (!std::is_same<TIn, float>::value) {
+        if (a.tstate) kern = replay_kernel<TIn, Lay, true>;
+    }
     if (geo.smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)geo.smem);

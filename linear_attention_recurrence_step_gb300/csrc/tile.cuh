@@ -61,11 +61,39 @@ __device__ __forceinline__ int64_t row_base4(int64_t n, int64_t Dv, int64_t dv, 
     return ((n * Dv + dv) * dk) >> 2;
 }
 
+// Four consecutive state entries of type TS as f32 (exact), and back
+// (rounded to nearest-even for 2-byte types): 16-byte pieces for f32, 8-byte
+// pieces otherwise, at the same entry positions.
+template <typename TS>
+__device__ __forceinline__ float4 ld_state4(const TS *p, int64_t i4) {
+    if constexpr (sizeof(TS) == 4) {
+        return __ldcs(reinterpret_cast<const float4 *>(p) + i4);
+    } else {
+        const uint2 raw = __ldcs(reinterpret_cast<const uint2 *>(p) + i4);
+        const TS *e = reinterpret_cast<const TS *>(&raw);
+        return make_float4(Elem<TS>::to_f32(e[0]), Elem<TS>::to_f32(e[1]), Elem<TS>::to_f32(e[2]),
+                           Elem<TS>::to_f32(e[3]));
+    }
+}
+template <typename TS>
+__device__ __forceinline__ void st_state4(TS *p, int64_t i4, float4 x) {
+    if constexpr (sizeof(TS) == 4) {
+        __stcs(reinterpret_cast<float4 *>(p) + i4, x);
+    } else {
+        uint2 raw;
+        TS *e = reinterpret_cast<TS *>(&raw);
+        e[0] = Elem<TS>::from_f32(x.x);
+        e[1] = Elem<TS>::from_f32(x.y);
+        e[2] = Elem<TS>::from_f32(x.z);
+        e[3] = Elem<TS>::from_f32(x.w);
+        __stcs(reinterpret_cast<uint2 *>(p) + i4, raw);
+    }
+}
+
 // Load this thread's rows of the tile (zeros for rows past Dv).
-template <class Lay>
-__device__ __forceinline__ void load_rows(Slice<Lay> &s, const float *state, int64_t n, int64_t Dv,
+template <class Lay, typename TS>
+__device__ __forceinline__ void load_rows(Slice<Lay> &s, const TS *state, int64_t n, int64_t Dv,
                                           int64_t row_first, int j) {
-    const float4 *p = reinterpret_cast<const float4 *>(state);
 #pragma unroll
     for (int m = 0; m < Lay::RT; ++m) {
         const int64_t dv = row_first + m;
@@ -73,15 +101,14 @@ __device__ __forceinline__ void load_rows(Slice<Lay> &s, const float *state, int
         const int64_t base = live ? row_base4(n, Dv, dv, Lay::DK) : 0;
 #pragma unroll
         for (int c = 0; c < Lay::NCH; ++c)
-            s[m][c] = live ? __ldcs(p + base + c * Lay::L + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            s[m][c] = live ? ld_state4(state, base + c * Lay::L + j) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
 // s <- s * G for the whole slice, then store rows < Dv (streaming stores).
-template <class Lay>
-__device__ __forceinline__ void store_rows(Slice<Lay> &s, float G, float *state, int64_t n,
+template <class Lay, typename TS>
+__device__ __forceinline__ void store_rows(Slice<Lay> &s, float G, TS *state, int64_t n,
                                            int64_t Dv, int64_t row_first, int j) {
-    float4 *p = reinterpret_cast<float4 *>(state);
     const float2 g2 = make_float2(G, G);
     const bool scale = G != 1.f;
 #pragma unroll
@@ -93,7 +120,7 @@ __device__ __forceinline__ void store_rows(Slice<Lay> &s, float G, float *state,
         for (int c = 0; c < Lay::NCH; ++c) {
             float4 x = s[m][c];
             if (scale) x = cat4(fmul2(lo2(x), g2), fmul2(hi2(x), g2));
-            __stcs(p + base + c * Lay::L + j, x);
+            st_state4(state, base + c * Lay::L + j, x);
         }
     }
 }

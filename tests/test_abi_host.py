@@ -56,7 +56,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libgdn.so does not export {name}"
-    assert lib.gdn_abi_version() == 5
+    assert lib.gdn_abi_version() == 6
 
 
 def test_library_is_sm103a():
@@ -175,6 +175,42 @@ def test_chunk_replay_rejects(lib, name):
     kw, want = CREPLAY_CASES[name]
     assert creplay(lib, **kw) == want
     assert lib.gdn_last_error().decode().startswith("gdn_chunk_replay")
+
+
+def rec_ts(lib, **kw):
+    args = dict(q=P(0), k=P(1), v=P(2), g=P(3), beta=P(4), state_in=P(5), mask=None,
+                y=P(6), state_out=P(7), delta_log=P(8), k_log=None, g_log=None,
+                B=2, T=3, Hk=2, Hv=4, Dk=64, Dv=32, mapping=0, dtype=BF16, stream=None)
+    args.update(kw)
+    return lib.gdn_step_record_tstate(*args.values())
+
+
+def rep_ts(lib, **kw):
+    args = dict(delta_log=P(0), k_log=P(1), g_log=P(2), state_in=P(3), mask=None,
+                state_out=P(4), B=2, T=3, Hv=4, Dk=64, Dv=32, accepted=2, per_seq=None,
+                dtype=BF16, stream=None)
+    args.update(kw)
+    return lib.gdn_state_replay_tstate(*args.values())
+
+
+TSTATE_CASES = {
+    "record mapping=5": (rec_ts, dict(mapping=5), INVALID),
+    "record state misaligned": (rec_ts, dict(state_in=P(5) + 8), MISALIGNED),
+    # bf16 state: 2 x 4 x 32 x 64 x 2 bytes = 32768; an 8-byte offset overlaps
+    "record state overlap": (rec_ts, dict(state_out=P(5) + 16), INVALID),
+    "record Dk=48": (rec_ts, dict(Dk=48), UNSUPPORTED),
+    "replay accepted<0": (rep_ts, dict(accepted=-3), INVALID),
+    "replay per_seq misaligned": (rep_ts, dict(per_seq=P(9) + 2), MISALIGNED),
+    "replay null g_log": (rep_ts, dict(g_log=None), INVALID),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TSTATE_CASES))
+def test_tstate_rejects(lib, name):
+    fn, kw, want = TSTATE_CASES[name]
+    assert fn(lib, **kw) == want
+    assert lib.gdn_last_error().decode().startswith(
+        "gdn_step_record_tstate" if fn is rec_ts else "gdn_state_replay_tstate")
 
 
 def rep_seq(lib, **kw):

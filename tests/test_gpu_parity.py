@@ -587,3 +587,45 @@ def test_chunk_replay_long_per_sequence_and_unused_slots(dev):
     gdn.gdn_chunk_replay(dtape, dkl, dgl, s1, mask, accepted=dacc, state_out=s1)
     torch.cuda.synchronize()
     assert torch.equal(s1, st)
+
+
+# ------------------------------------------------ state stored in T
+@pytest.mark.parametrize("dtype,Dk,T", [("bf16", 128, 16), ("bf16", 64, 37), ("bf16", 128, 5),
+                                         ("f16", 128, 16), ("f16", 64, 9)])
+def test_state_in_t(dev, dtype, Dk, T):
+    """gdn_step_record_tstate / gdn_state_replay_tstate: the state stored in
+    the input type (widened on load, rounded once on store), the tensor-core
+    record (bf16, T >= 12) and the FP32 kernels, then the replay of a
+    host-made tape from the same stored snapshot (single and per-sequence
+    counts)."""
+    case = workloads.make_case(B=3, T=T, Hk=2, Hv=4, Dk=Dk, Dv=72, dtype=dtype, seed=950 + T,
+                               mask="bernoulli:0.8", accepted="uniform")
+    s_store = workloads.to_storage(case.state, dtype)
+    s64 = workloads.widen(s_store, dtype)
+    q, k, v, g, beta, _, mask = device_inputs(case, dev)
+    s0 = to_dev(s_store, dev)
+    out = _alloc_outputs(case, dev)
+    out["state_out"] = torch.full_like(s0, float("nan"))
+    gdn.gdn_step_record(q, k, v, g, beta, s0, mask, **out)
+    torch.cuda.synchronize()
+    assert out["state_out"].dtype == s0.dtype
+    q64, k64, v64, g64, b64, _, m = _oracle_inputs(case)
+    ref = oracle.record(q64, k64, v64, g64, b64, s64, m)
+    got = dict(out)
+    act = _active(case)
+    assert_close(to_host_f64(got["state_out"]), ref["state_out"], dtype, dtype, "state_out (stored in T)")
+    assert_close(to_host_f64(got["y"])[act], ref["y"][act], dtype, dtype, "y")
+    assert_close(to_host_f64(got["delta_log"])[act], ref["delta_log"][act], dtype, dtype, "delta_log")
+    tape, kl, gl = _host_tape(case, ref)
+    dtape, dkl, dgl = to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev)
+    st = gdn.gdn_state_replay(dtape, dkl, dgl, s0, mask, accepted=case.accepted)
+    want = oracle.replay(workloads.widen(tape, dtype), workloads.widen(kl, dtype),
+                         workloads.widen(gl, dtype), s64, case.mask, accepted=case.accepted)
+    assert st.dtype == s0.dtype
+    assert_close(to_host_f64(st), want, dtype, dtype, "replay (state in T)")
+    acc = np.array([0, T, T // 2], dtype=np.int32)
+    st2 = gdn.gdn_state_replay(dtape, dkl, dgl, s0, mask, accepted=torch.from_numpy(acc).to(dev))
+    want2 = oracle.replay(workloads.widen(tape, dtype), workloads.widen(kl, dtype),
+                          workloads.widen(gl, dtype), s64, case.mask, accepted=acc.astype(np.int64))
+    assert_close(to_host_f64(st2), want2, dtype, dtype, "per-sequence replay (state in T)")
+    assert torch.equal(st2[0], s0[0])
