@@ -68,9 +68,10 @@ __host__ __device__ constexpr size_t chunk_scan_smem_bytes(int dk, int esize) {
            (size_t)2 * kCkWarps * kCkRows * kCkPartStride * 4 +
            (size_t)2 * kCkC * kCkOutStride * 4;
 }
+constexpr int kCkHeadsPerPass = 4;  // value heads of one key head processed side by side
 __host__ __device__ constexpr size_t chunk_local_smem_bytes(int dk) {
-    return (size_t)2 * kCkC * (dk + 4) * 4 + (size_t)4 * kCkC * (kCkC + 1) * 4 +
-           (size_t)3 * kCkC * 4;
+    return (size_t)2 * kCkC * (dk + 4) * 4 + (size_t)(2 + 2 * kCkHeadsPerPass) * kCkC * (kCkC + 1) * 4 +
+           (size_t)3 * kCkHeadsPerPass * kCkC * 4;
 }
 
 // ------------------------------------------------------------ tf32 products
@@ -197,11 +198,12 @@ chunk_local_kernel(const ChunkArgs a) {
     float *sq = sk + C * KS;
     float *sKK = sq + C * KS;    // k_t . k_u
     float *sKQ = sKK + C * CS;   // k_u . q_t
-    float *sA = sKQ + C * CS;    // A[t][u], u <= t (zero above)
-    float *sN = sA + C * CS;     // N[t][u], u < t (zero elsewhere)
-    float *sg = sN + C * CS;     // effective g (1 on inactive steps)
-    float *sb = sg + C;          // effective beta (0 on inactive steps)
-    float *sG = sb + C;          // Gam_t
+    constexpr int HP = kCkHeadsPerPass;
+    float *sA = sKQ + C * CS;    // [HP][C][CS] A[t][u], u <= t (zero above)
+    float *sN = sA + HP * C * CS;  // [HP][C][CS] N[t][u], u < t (zero elsewhere)
+    float *sg = sN + HP * C * CS;  // [HP][C] effective g (1 on inactive steps)
+    float *sb = sg + HP * C;       // [HP][C] effective beta (0 on inactive steps)
+    float *sG = sb + HP * C;       // [HP][C] Gam_t
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int64_t nch = a.nchunks;
@@ -254,69 +256,88 @@ chunk_local_kernel(const ChunkArgs a) {
         sKQ[t * CS + u] = kq;
     }
 
-    for (int64_t i = 0; i < G; ++i) {
-        const int64_t hv = a.tiled_gqa ? hk + i * a.Hk : hk * G + i;
-        const int64_t n = b * a.Hv + hv;
-        if (tid < C) {
-            const bool on = (bits >> tid) & 1u;
-            const int64_t gi = (b * a.T + t0 + tid) * a.Hv + hv;
-            sg[tid] = on ? ld_f32(gp + gi) : 1.f;
-            sb[tid] = on ? ld_f32(bp + gi) : 0.f;
+    // the value heads that read key head hk, up to kCkHeadsPerPass at a time:
+    // decay products, the inverse and the workspace block of each head run
+    // side by side (one 16-thread group per head for the inverse)
+    for (int64_t i0 = 0; i0 < G; i0 += kCkHeadsPerPass) {
+        const int nh = (int)min((int64_t)kCkHeadsPerPass, G - i0);
+        auto hv_of = [&](int i) { return a.tiled_gqa ? hk + (i0 + i) * a.Hk : hk * G + i0 + i; };
+        if (tid < nh * C) {
+            const int i = tid / C, tt = tid - i * C;
+            const bool on = (bits >> tt) & 1u;
+            const int64_t gi = (b * a.T + t0 + tt) * a.Hv + hv_of(i);
+            sg[i * C + tt] = on ? ld_f32(gp + gi) : 1.f;
+            sb[i * C + tt] = on ? ld_f32(bp + gi) : 0.f;
         }
-        __syncthreads();  // g, beta of this head; Gram entries (first pass)
-        {
-            const int t = tid >> 4, u = tid & 15;
+        __syncthreads();  // g, beta of these heads; Gram entries (first pass)
+        for (int e = tid; e < nh * C * C; e += kCkLocalThreads) {
+            const int i = e / (C * C), t = (e >> 4) & 15, u = e & 15;
+            const float *gh = sg + i * C;
             float p = 1.f;
-            for (int x = u + 1; x <= t; ++x) p *= sg[x];
-            sA[t * CS + u] = u <= t ? p : 0.f;
-            sN[t * CS + u] = u < t ? sb[t] * p * sKK[t * CS + u] : 0.f;
+            for (int x = u + 1; x <= t; ++x) p *= gh[x];
+            sA[(i * C + t) * CS + u] = u <= t ? p : 0.f;
+            sN[(i * C + t) * CS + u] = u < t ? sb[i * C + t] * p * sKK[t * CS + u] : 0.f;
             if (u == 0) {
                 float Gm = 1.f;
-                for (int x = 0; x <= t; ++x) Gm *= sg[x];
-                sG[t] = Gm;
+                for (int x = 0; x <= t; ++x) Gm *= gh[x];
+                sG[i * C + t] = Gm;
             }
         }
         __syncthreads();
 
-        float *ws = a.workspace + (n * nch + c) * kCkWsFloats;
-        if (tid < C) {
-            // W = (I + N)^-1, one column u per thread, held in registers:
+        if (tid < nh * C) {
+            // W = (I + N)^-1 of head i, one column u per thread, held in registers:
             // W[t][u] = -sum_{x < t} N[t][x] W[x][u]  (W[x][u] = 0 for x < u)
-            const int u = tid;
+            const int i = tid / C, u = tid - i * C;
+            const float *Nh = sN + i * C * CS;
             float w[C];
 #pragma unroll
             for (int t = 0; t < C; ++t) {
                 float acc = 0.f;
 #pragma unroll
-                for (int x = 0; x < t; ++x) acc = fmaf(sN[t * CS + x], w[x], acc);
+                for (int x = 0; x < t; ++x) acc = fmaf(Nh[t * CS + x], w[x], acc);
                 w[t] = t < u ? 0.f : (t == u ? 1.f : -acc);
             }
-            const float bu = sb[u];
+            const float bu = sb[i * C + u];
+            float *ws = a.workspace + ((b * a.Hv + hv_of(i)) * nch + c) * kCkWsFloats;
 #pragma unroll
             for (int t = 0; t < C; ++t) ws[t * C + u] = w[t] * bu;  // Wb
-        } else {
-            for (int j = tid - C; j < C * C; j += kCkLocalThreads - C) {
-                const int t = j >> 4, u = j & 15;
-                ws[C * C + j] = u <= t ? sA[t * CS + u] * sKQ[t * CS + u] : 0.f;  // Mq
+        }
+        const int ft = tid - nh * C;  // the other threads: Mq, Gam, aC, tape capture
+        if (ft >= 0) {
+            const int nf = kCkLocalThreads - nh * C;
+            for (int e = ft; e < nh * C * C; e += nf) {
+                const int i = e / (C * C), j = e - i * C * C, t = j >> 4, u = j & 15;
+                float *ws = a.workspace + ((b * a.Hv + hv_of(i)) * nch + c) * kCkWsFloats;
+                ws[C * C + j] = u <= t ? sA[(i * C + t) * CS + u] * sKQ[t * CS + u] : 0.f;  // Mq
             }
-            if (tid >= 2 * C && tid < 3 * C) ws[2 * C * C + tid - 2 * C] = sG[tid - 2 * C];      // Gam
-            if (tid >= 3 * C && tid < 4 * C) ws[2 * C * C + C + tid - 3 * C] = sA[(C - 1) * CS + tid - 3 * C];  // aC
+            for (int e = ft; e < nh * 2 * C; e += nf) {
+                const int i = e / (2 * C), j = e - i * 2 * C;
+                float *ws = a.workspace + ((b * a.Hv + hv_of(i)) * nch + c) * kCkWsFloats;
+                ws[2 * C * C + j] = j < C ? sG[i * C + j] : sA[(i * C + C - 1) * CS + (j - C)];  // Gam, aC
+            }
             // tape capture: k_log rows and g_log of the active steps
             if (a.k_log) {
                 TIn *klp = static_cast<TIn *>(a.k_log);
-                for (int j = tid - C; j < C * DK / VEC; j += kCkLocalThreads - C) {
+                for (int e = ft; e < nh * C * DK / VEC; e += nf) {
+                    const int i = e / (C * DK / VEC), j = e - i * (C * DK / VEC);
                     const int tt = j / (DK / VEC), x = (j - tt * (DK / VEC)) * VEC;
                     if ((bits >> tt) & 1u)
-                        *reinterpret_cast<uint4 *>(klp + ((b * a.T + t0 + tt) * a.Hv + hv) * DK + x) =
+                        *reinterpret_cast<uint4 *>(klp + ((b * a.T + t0 + tt) * a.Hv + hv_of(i)) * DK + x) =
                             *reinterpret_cast<const uint4 *>(kp + ((b * a.T + t0 + tt) * a.Hk + hk) * DK + x);
                 }
             }
-            if (a.g_log && tid >= C && tid < C + tcnt && ((bits >> (tid - C)) & 1u)) {
-                const int64_t gi = (b * a.T + t0 + tid - C) * a.Hv + hv;
-                static_cast<TIn *>(a.g_log)[gi] = gp[gi];
+            if (a.g_log) {
+                for (int e = ft; e < nh * C; e += nf) {
+                    const int i = e / C, tt = e - i * C;
+                    if (tt < tcnt && ((bits >> tt) & 1u)) {
+                        const int64_t gi = (b * a.T + t0 + tt) * a.Hv + hv_of(i);
+                        static_cast<TIn *>(a.g_log)[gi] = gp[gi];
+                    }
+                }
             }
         }
-        __syncthreads();  // sg / sb / sA / sN are rewritten for the next head
+        __syncthreads();  // sg / sb / sA / sN are rewritten for the next heads
     }
 }
 
