@@ -37,7 +37,7 @@ import numpy as np
 DTYPES = ("f32", "bf16", "f16")
 
 # Named workloads.  Sizes, distributions and structure are the five
-# configurations the GB300 build is measured and checked on.
+# configurations this library is measured and checked on.
 CONFIGS: Dict[str, dict] = {
     # tiny f32 parity case: record then replay with accepted=3
     "tiny_f32": dict(B=1, T=4, Hk=2, Hv=4, Dk=32, Dv=32, dtype="f32",
