@@ -105,11 +105,8 @@ static int max_warps(int dk) {
     return 1;
 }
 
-// Warps per CTA: at most kMaxWarpsPerCta (smaller CTAs, more of them per SM:
-// their load, compute and store phases overlap better -- measured 6 % faster
-// replay and 9 % faster decode record than whole-tile CTAs of 8 warps), fewer
-// (rows of a tile split over more CTAs) when the tiles are few.
-static constexpr int kMaxWarpsPerCta = 4;
+// Warps per CTA: at most kMaxWarpsPerCta (launch.h), fewer (rows of a tile
+// split over more CTAs) when the tiles are few.
 static int pick_warps(int dk, int rw, int64_t tiles, int64_t Dv, int sm_count) {
     int nw = (int)std::min<int64_t>(std::min(max_warps(dk), kMaxWarpsPerCta), ceil_div(Dv, rw));
     const int64_t want = 2 * (int64_t)(sm_count > 0 ? sm_count : 1);

@@ -9,6 +9,12 @@ namespace gdn {
 
 enum class DType : int { F32 = 0, BF16 = 1, F16 = 2 };
 
+// Warps per CTA of the FP32 record and replay kernels: smaller CTAs, more of
+// them per SM, overlap their load, compute and store phases better (measured
+// 6 % faster replay and 9 % faster decode record than whole-tile CTAs of
+// eight warps).
+constexpr int kMaxWarpsPerCta = 4;
+
 // Launch geometry chosen on the host: each CTA owns `rows_cta` consecutive
 // value rows (dv) of one (b, hv) state tile; `row_blocks` CTAs cover a tile;
 // `tc` timesteps are staged in shared memory at a time.
