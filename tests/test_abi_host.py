@@ -125,6 +125,10 @@ CHUNK_CASES = {
     "dtype": (dict(dtype=7), UNSUPPORTED),
     "q misaligned": (dict(q=P(0) + 4), MISALIGNED),
     "state overlap": (dict(state_out=P(5) + 16), INVALID),
+    # more CTAs than a grid holds (2^31 - 1) is refused, not launched short:
+    # 2^30 chunks of 16 steps, or 2^30 blocks of 16 rows, for 4 value heads
+    "grid chunks": (dict(T=16 << 30, state_out=P(5), workspace_bytes=1 << 50), INVALID),
+    "grid rows": (dict(Dv=16 << 30, state_out=P(5), workspace_bytes=1 << 50), INVALID),
 }
 
 
@@ -136,6 +140,8 @@ def test_chunk_prefill_rejects(lib, name):
     assert msg.startswith("gdn_chunk_prefill")
     if name == "workspace too small":
         assert "need 17408 bytes, have 100" in msg  # 2 x 4 x 1 x 544 x 4
+    if name.startswith("grid"):
+        assert "grid too large" in msg
 
 
 def creplay(lib, **kw):
@@ -167,6 +173,8 @@ CREPLAY_CASES = {
     "state misaligned": (dict(state_in=P(3) + 4), MISALIGNED),
     "per_seq misaligned": (dict(per_seq=P(10) + 2), MISALIGNED),
     "state overlap": (dict(state_out=P(3) + 16), INVALID),
+    # 2^32 (b, hv) tiles: more CTAs than a grid holds
+    "grid tiles": (dict(B=1 << 20, Hv=1 << 12, state_out=P(3), workspace_bytes=1 << 62), INVALID),
 }
 
 
@@ -174,7 +182,10 @@ CREPLAY_CASES = {
 def test_chunk_replay_rejects(lib, name):
     kw, want = CREPLAY_CASES[name]
     assert creplay(lib, **kw) == want
-    assert lib.gdn_last_error().decode().startswith("gdn_chunk_replay")
+    msg = lib.gdn_last_error().decode()
+    assert msg.startswith("gdn_chunk_replay")
+    if name.startswith("grid"):
+        assert "grid too large" in msg
 
 
 def rec_ts(lib, **kw):
