@@ -13,9 +13,9 @@ cudaError_t launch_replay_tc(DType dt, int dk, const ReplayTcArgs &a, cudaStream
     return cudaErrorInvalidValue;
 }
 
-// Steps are split over CTAs only when the tiles alone give fewer than 128
-// CTAs; the plan depends on the shapes only (not on the device), so the
-// workspace size is a pure function of them.
+// Steps are split over CTAs only when the tiles alone give fewer than
+// 128 x (CTAs per SM) CTAs; the plan depends on the shapes only (not on the
+// device), so the workspace size is a pure function of them.
 ReplayTcPlan replay_tc_plan(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv) {
     ReplayTcPlan p{};
     p.bytes = -1;
@@ -23,7 +23,8 @@ ReplayTcPlan replay_tc_plan(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_
     int64_t items = 0, nkb = (T + kTcSteps - 1) / kTcSteps;
     if (__builtin_mul_overflow(B, Hv, &items) || __builtin_mul_overflow(items, p.row_blocks, &items))
         return p;
-    int64_t splits = items >= 128 ? 1 : std::min<int64_t>(nkb, 128 / items);
+    const int64_t want = 128 * (int64_t)tc_ctas_per_sm((int)Dk);
+    int64_t splits = items >= want ? 1 : std::min<int64_t>(nkb, want / items);
     if (splits < 1) splits = 1;
     p.split_steps = ((nkb + splits - 1) / splits) * kTcSteps;
     p.splits = (int)((T + p.split_steps - 1) / p.split_steps);
