@@ -213,29 +213,61 @@ chunk_local_kernel(const ChunkArgs a) {
     const int64_t G = a.Hv / a.Hk;
     const int64_t t0 = c * C;
     const int tcnt = (int)min((int64_t)C, a.T - t0);
-    const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
+    auto hv_at = [&](int64_t h) { return a.tiled_gqa ? hk + h * a.Hk : hk * G + h; };
 
     const TIn *kp = static_cast<const TIn *>(a.k);
     const TIn *qp = static_cast<const TIn *>(a.q);
     const TIn *gp = static_cast<const TIn *>(a.g);
     const TIn *bp = static_cast<const TIn *>(a.beta);
 
-    // k / q rows of active steps, widened; rows of inactive steps are zero
-    for (int i = tid; i < C * DK / VEC; i += kCkLocalThreads) {
-        const int tt = i / (DK / VEC), x = (i - tt * (DK / VEC)) * VEC;
-        float kv[VEC], qv[VEC];
-        if ((bits >> tt) & 1u) {
-            const int64_t off = ((b * a.T + t0 + tt) * a.Hk + hk) * DK + x;
-            widen_piece<TIn>(*reinterpret_cast<const uint4 *>(kp + off), kv);
-            widen_piece<TIn>(*reinterpret_cast<const uint4 *>(qp + off), qv);
-        } else {
+    // ---- every load of the chunk is issued before any of them is waited
+    // for: the k / q pieces of the steps inside the call, g and beta of the
+    // first pass of value heads, then the mask words.
+    constexpr int NPIECE = C * DK / VEC;  // 16-byte pieces of a chunk's k (or q) rows
+    constexpr int NPC = (NPIECE + kCkLocalThreads - 1) / kCkLocalThreads;
+    uint4 kraw[NPC], qraw[NPC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) kv[e] = qv[e] = 0.f;
+    for (int j = 0; j < NPC; ++j) {
+        const int i = tid + j * kCkLocalThreads;
+        kraw[j] = qraw[j] = make_uint4(0u, 0u, 0u, 0u);
+        const int tt = i / (DK / VEC), x = (i - tt * (DK / VEC)) * VEC;
+        if (i < NPIECE && tt < tcnt) {
+            const int64_t off = ((b * a.T + t0 + tt) * a.Hk + hk) * DK + x;
+            kraw[j] = *reinterpret_cast<const uint4 *>(kp + off);
+            qraw[j] = *reinterpret_cast<const uint4 *>(qp + off);
         }
+    }
+    const int nh0 = (int)min((int64_t)kCkHeadsPerPass, G);
+    TIn g0 = Elem<TIn>::from_f32(1.f), b0 = Elem<TIn>::from_f32(0.f);
+    if (tid < nh0 * C && tid % C < tcnt) {
+        const int64_t gi = (b * a.T + t0 + tid % C) * a.Hv + hv_at(tid / C);
+        g0 = gp[gi];
+        b0 = bp[gi];
+    }
+    const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
+
+    // k / q rows widened into shared memory (rows of inactive steps zero);
+    // k_log rows of the active steps copied bit for bit from the same pieces
+#pragma unroll
+    for (int j = 0; j < NPC; ++j) {
+        const int i = tid + j * kCkLocalThreads;
+        if (i >= NPIECE) break;
+        const int tt = i / (DK / VEC), x = (i - tt * (DK / VEC)) * VEC;
+        const bool on = (bits >> tt) & 1u;
+        float kv[VEC], qv[VEC];
+        widen_piece<TIn>(kraw[j], kv);
+        widen_piece<TIn>(qraw[j], qv);
 #pragma unroll
         for (int e = 0; e < VEC; e += 4) {
-            *reinterpret_cast<float4 *>(sk + tt * KS + x + e) = make_float4(kv[e], kv[e + 1], kv[e + 2], kv[e + 3]);
-            *reinterpret_cast<float4 *>(sq + tt * KS + x + e) = make_float4(qv[e], qv[e + 1], qv[e + 2], qv[e + 3]);
+            *reinterpret_cast<float4 *>(sk + tt * KS + x + e) =
+                on ? make_float4(kv[e], kv[e + 1], kv[e + 2], kv[e + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4 *>(sq + tt * KS + x + e) =
+                on ? make_float4(qv[e], qv[e + 1], qv[e + 2], qv[e + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (a.k_log && on) {
+            TIn *klp = static_cast<TIn *>(a.k_log);
+            for (int64_t h = 0; h < G; ++h)
+                *reinterpret_cast<uint4 *>(klp + ((b * a.T + t0 + tt) * a.Hv + hv_at(h)) * DK + x) = kraw[j];
         }
     }
     __syncthreads();
@@ -261,13 +293,18 @@ chunk_local_kernel(const ChunkArgs a) {
     // side by side (one 16-thread group per head for the inverse)
     for (int64_t i0 = 0; i0 < G; i0 += kCkHeadsPerPass) {
         const int nh = (int)min((int64_t)kCkHeadsPerPass, G - i0);
-        auto hv_of = [&](int i) { return a.tiled_gqa ? hk + (i0 + i) * a.Hk : hk * G + i0 + i; };
+        auto hv_of = [&](int i) { return hv_at(i0 + i); };
         if (tid < nh * C) {
+            // g and beta of the pass (the first pass's were loaded up front);
+            // g_log of the active steps
             const int i = tid / C, tt = tid - i * C;
             const bool on = (bits >> tt) & 1u;
             const int64_t gi = (b * a.T + t0 + tt) * a.Hv + hv_of(i);
-            sg[i * C + tt] = on ? ld_f32(gp + gi) : 1.f;
-            sb[i * C + tt] = on ? ld_f32(bp + gi) : 0.f;
+            const TIn gr = i0 == 0 ? g0 : (on ? gp[gi] : g0);
+            const TIn br = i0 == 0 ? b0 : (on ? bp[gi] : b0);
+            sg[i * C + tt] = on ? Elem<TIn>::to_f32(gr) : 1.f;
+            sb[i * C + tt] = on ? Elem<TIn>::to_f32(br) : 0.f;
+            if (a.g_log && on) static_cast<TIn *>(a.g_log)[gi] = gr;
         }
         __syncthreads();  // g, beta of these heads; Gram entries (first pass)
         for (int e = tid; e < nh * C * C; e += kCkLocalThreads) {
@@ -303,7 +340,7 @@ chunk_local_kernel(const ChunkArgs a) {
 #pragma unroll
             for (int t = 0; t < C; ++t) ws[t * C + u] = w[t] * bu;  // Wb
         }
-        const int ft = tid - nh * C;  // the other threads: Mq, Gam, aC, tape capture
+        const int ft = tid - nh * C;  // the other threads: Mq, Gam, aC
         if (ft >= 0) {
             const int nf = kCkLocalThreads - nh * C;
             for (int e = ft; e < nh * C * C; e += nf) {
@@ -315,26 +352,6 @@ chunk_local_kernel(const ChunkArgs a) {
                 const int i = e / (2 * C), j = e - i * 2 * C;
                 float *ws = a.workspace + ((b * a.Hv + hv_of(i)) * nch + c) * kCkWsFloats;
                 ws[2 * C * C + j] = j < C ? sG[i * C + j] : sA[(i * C + C - 1) * CS + (j - C)];  // Gam, aC
-            }
-            // tape capture: k_log rows and g_log of the active steps
-            if (a.k_log) {
-                TIn *klp = static_cast<TIn *>(a.k_log);
-                for (int e = ft; e < nh * C * DK / VEC; e += nf) {
-                    const int i = e / (C * DK / VEC), j = e - i * (C * DK / VEC);
-                    const int tt = j / (DK / VEC), x = (j - tt * (DK / VEC)) * VEC;
-                    if ((bits >> tt) & 1u)
-                        *reinterpret_cast<uint4 *>(klp + ((b * a.T + t0 + tt) * a.Hv + hv_of(i)) * DK + x) =
-                            *reinterpret_cast<const uint4 *>(kp + ((b * a.T + t0 + tt) * a.Hk + hk) * DK + x);
-                }
-            }
-            if (a.g_log) {
-                for (int e = ft; e < nh * C; e += nf) {
-                    const int i = e / C, tt = e - i * C;
-                    if (tt < tcnt && ((bits >> tt) & 1u)) {
-                        const int64_t gi = (b * a.T + t0 + tt) * a.Hv + hv_of(i);
-                        static_cast<TIn *>(a.g_log)[gi] = gp[gi];
-                    }
-                }
             }
         }
         __syncthreads();  // sg / sb / sA / sN are rewritten for the next heads
