@@ -164,6 +164,11 @@ def _sweep_cases():
         mask = ["none", "bernoulli:0.6", "prefix", "all_on"][i % 4]
         cases.append(dict(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, dtype=dt, seed=500 + i,
                           mask=mask, accepted="uniform"))
+    # the Dk = 64, Dv = 32 cell of the record page's test list, every dtype
+    # (bf16 at T >= 12 takes the tensor-core record)
+    for j, (dt, T) in enumerate((("f32", 8), ("bf16", 16), ("f16", 21))):
+        cases.append(dict(B=2, T=T, Hk=2, Hv=4, Dk=64, Dv=32, dtype=dt, seed=530 + j,
+                          mask="bernoulli:0.7", accepted="uniform"))
     return cases
 
 
