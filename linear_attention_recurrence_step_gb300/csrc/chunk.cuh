@@ -33,9 +33,11 @@
 // Work split: a CTA owns 16 state rows of one (b, hv) tile and four warps
 // split the Dk columns (each holds 16 rows x Dk/4 of the state).  The partial
 // products P of the four warps are summed through shared memory once per
-// chunk; that exchange is the kernel's only CTA barrier per chunk.  Inputs of
-// chunk c+2 are copied with cp.async into a three-slot ring while chunk c is
-// computed, so the barrier of chunk c also publishes chunk c+1.
+// chunk; that exchange is the kernel's only CTA barrier per chunk.  The
+// outputs are spread over the warps: two write the delta_log rows and two
+// the y rows, eight steps each.  Inputs of chunk c+2 are copied with
+// cp.async into a three-slot ring while chunk c is computed, so the barrier
+// of chunk c also publishes chunk c+1.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -90,14 +92,6 @@ __device__ __forceinline__ void mma_tf32_1688(float (&d)[4], const uint32_t (&a)
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// d += a b in three tf32 products, small terms first.
-__device__ __forceinline__ void mma3_tf32(float (&d)[4], const uint32_t (&ah)[4],
-                                          const uint32_t (&al)[4], uint32_t bh0, uint32_t bh1,
-                                          uint32_t bl0, uint32_t bl1) {
-    mma_tf32_1688(d, al, bh0, bh1);
-    mma_tf32_1688(d, ah, bl0, bl1);
-    mma_tf32_1688(d, ah, bh0, bh1);
 }
 
 // An m16n8 accumulator fragment (lane = 4 g + t holds rows g, g+8 and columns
@@ -395,7 +389,7 @@ chunk_scan_kernel(const ChunkArgs a) {
     auto slotV = [&](int sl) { return reinterpret_cast<TIn *>(smem + sl * kSlot + kOffV); };
     auto slotW = [&](int sl) { return reinterpret_cast<float *>(smem + sl * kSlot + kOffW); };
     float *part = reinterpret_cast<float *>(smem + 3 * kSlot);         // [2][warps][16][PS]
-    float *otile = part + 2 * kCkWarps * kCkRows * PS;                 // [2][16 steps][OS]
+    float *otile = part + 2 * kCkWarps * kCkRows * PS;                 // [4 warps][8 steps][OS]
 
     const TIn *qp = static_cast<const TIn *>(a.q);
     const TIn *kp = static_cast<const TIn *>(a.k);
@@ -478,11 +472,16 @@ chunk_scan_kernel(const ChunkArgs a) {
     cp_async_wait_group<1>();
     __syncthreads();
 
+    // Outputs of a chunk, spread over the four warps: warp w writes the
+    // delta_log (w < 2) or y (w >= 2) rows of steps 8 (w & 1) .. 8 (w & 1) + 7.
+    static_assert(kCkWarps == 4, "the output roles assume four warps");
     TIn *yp = static_cast<TIn *>(a.y);
     TIn *dp = static_cast<TIn *>(a.delta_log);
-    const bool out_warp = warp == 0 || (warp == 1 && dp);  // y: warp 0; delta_log: warp 1
-    TIn *const outp = warp == 0 ? yp : dp;
-    float *const mytile = otile + (warp & 1) * C * OS;
+    const bool ywarp = warp >= 2;
+    const int oh = warp & 1;  // this warp's n-tile: steps 8 oh .. 8 oh + 7
+    const bool out_warp = ywarp || dp != nullptr;
+    TIn *const outp = ywarp ? yp : dp;
+    float *const mytile = otile + warp * 8 * OS;
 
     int sl = 0, sl2 = 2;  // ring slots of chunks c and c + 2
     for (int64_t c = 0; c < nch; ++c) {
@@ -530,11 +529,10 @@ chunk_scan_kernel(const ChunkArgs a) {
         __syncthreads();  // partials of chunk c and the inputs of chunk c+1 are visible
         issue(c + 2, sl2);
 
-        // ---- sum the four partials and scale by Gam (P_k for every warp, P_q
-        // for the y warp)
+        // ---- sum the four partials and scale by Gam (P_k for every warp; the
+        // y warps also P_q of their n-tile)
         const float *pc = part + (c & 1) * kCkWarps * kCkRows * PS;
-        const bool ywarp = warp == 0;
-        float Pk[2][4] = {}, Pq[2][4] = {};
+        float Pk[2][4] = {}, Pq[4] = {};
 #pragma unroll
         for (int w = 0; w < kCkWarps; ++w) {
             const float *pw = pc + w * kCkRows * PS;
@@ -546,15 +544,14 @@ chunk_scan_kernel(const ChunkArgs a) {
                 Pk[nt][1] += u0.y;
                 Pk[nt][2] += u1.x;
                 Pk[nt][3] += u1.y;
-                if (ywarp) {
-                    const float2 w0 = *reinterpret_cast<const float2 *>(pw + g * PS + 16 + 8 * nt + 2 * t);
-                    const float2 w1 =
-                        *reinterpret_cast<const float2 *>(pw + (g + 8) * PS + 16 + 8 * nt + 2 * t);
-                    Pq[nt][0] += w0.x;
-                    Pq[nt][1] += w0.y;
-                    Pq[nt][2] += w1.x;
-                    Pq[nt][3] += w1.y;
-                }
+            }
+            if (ywarp) {
+                const float2 w0 = *reinterpret_cast<const float2 *>(pw + g * PS + 16 + 8 * oh + 2 * t);
+                const float2 w1 = *reinterpret_cast<const float2 *>(pw + (g + 8) * PS + 16 + 8 * oh + 2 * t);
+                Pq[0] += w0.x;
+                Pq[1] += w0.y;
+                Pq[2] += w1.x;
+                Pq[3] += w1.y;
             }
         }
 #pragma unroll
@@ -564,10 +561,13 @@ chunk_scan_kernel(const ChunkArgs a) {
             Pk[nt][1] *= gm.y;
             Pk[nt][2] *= gm.x;
             Pk[nt][3] *= gm.y;
-            Pq[nt][0] *= gm.x;
-            Pq[nt][1] *= gm.y;
-            Pq[nt][2] *= gm.x;
-            Pq[nt][3] *= gm.y;
+        }
+        {
+            const float2 gm = *reinterpret_cast<const float2 *>(Gam + 8 * oh + 2 * t);
+            Pq[0] *= gm.x;
+            Pq[1] *= gm.y;
+            Pq[2] *= gm.x;
+            Pq[3] *= gm.y;
         }
 
         // ---- R = V^T - P_k;  D = R Wb^T (every warp: D is MMA-2's A operand)
@@ -606,44 +606,45 @@ chunk_scan_kernel(const ChunkArgs a) {
 
         const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
         if (out_warp) {
+            float o[4];
             if (ywarp) {
-                // ---- Y = P_q + D Mq^T
+                // ---- Y = P_q + D Mq^T for this warp's n-tile
                 uint32_t dh[2][4], dl[2][4];
                 acc_as_a(D[0], dh[0], dl[0]);
                 acc_as_a(D[1], dh[1], dl[1]);
+                // the three tf32 terms in separate accumulators (two-deep chains)
+                float Ym[4] = {}, Ya[4] = {}, Yb[4] = {};
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const float2 mq = *reinterpret_cast<const float2 *>(Mq + (8 * nt + g) * C + 8 * i + 2 * t);
-                        uint32_t bh0, bl0, bh1, bl1;
-                        split_tf32(mq.x, bh0, bl0);
-                        split_tf32(mq.y, bh1, bl1);
-                        mma3_tf32(Pq[nt], dh[i], dl[i], bh0, bh1, bl0, bl1);
-                    }
+                for (int i = 0; i < 2; ++i) {
+                    const float2 mq = *reinterpret_cast<const float2 *>(Mq + (8 * oh + g) * C + 8 * i + 2 * t);
+                    uint32_t bh0, bl0, bh1, bl1;
+                    split_tf32(mq.x, bh0, bl0);
+                    split_tf32(mq.y, bh1, bl1);
+                    mma_tf32_1688(Ya, dl[i], bh0, bh1);
+                    mma_tf32_1688(Yb, dh[i], bl0, bl1);
+                    mma_tf32_1688(Ym, dh[i], bh0, bh1);
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = Pq[e] + (Ym[e] + (Ya[e] + Yb[e]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = oh ? D[1][e] : D[0][e];
             }
-            // stage the 16 steps x 16 rows tile, then store whole step rows
+            // stage the 8 steps x 16 rows tile, then store whole step rows
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    mytile[(8 * nt + 2 * t + (e & 1)) * OS + g + 8 * (e >> 1)] = ywarp ? Pq[nt][e] : D[nt][e];
+            for (int e = 0; e < 4; ++e) mytile[(2 * t + (e & 1)) * OS + g + 8 * (e >> 1)] = o[e];
             __syncwarp();
             if (a.vec_out && vlim == kCkRows) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int s = 8 * h + (lane >> 2), x = 4 * (lane & 3);
-                    if (s < tcnt && ((bits >> s) & 1u))
-                        st4<TIn>(outp + ((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + x,
-                                 *reinterpret_cast<const float4 *>(mytile + s * OS + x));
-                }
+                const int sl8 = lane >> 2, x = 4 * (lane & 3), s = 8 * oh + sl8;
+                if (s < tcnt && ((bits >> s) & 1u))
+                    st4<TIn>(outp + ((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + x,
+                             *reinterpret_cast<const float4 *>(mytile + sl8 * OS + x));
             } else {
-                for (int i = lane; i < C * kCkRows; i += 32) {
-                    const int s = i / kCkRows, r = i - s * kCkRows;
+                for (int i = lane; i < 8 * kCkRows; i += 32) {
+                    const int sl8 = i / kCkRows, r = i - sl8 * kCkRows, s = 8 * oh + sl8;
                     if (s < tcnt && ((bits >> s) & 1u) && r < vlim)
                         outp[((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + r] =
-                            Elem<TIn>::from_f32(mytile[s * OS + r]);
+                            Elem<TIn>::from_f32(mytile[sl8 * OS + r]);
                 }
             }
             __syncwarp();
