@@ -348,7 +348,6 @@ gdn_status chunk_prefill_impl(const char *fn, const void *q, const void *k, cons
     a.nchunks = ceil_div(T, gdn::kCkC);
     a.row_blocks = ceil_div(Dv, gdn::kCkRows);
     a.vec_v = aligned(v, 16) && (Dv * eb) % 16 == 0;
-    a.vec_out = Dv % 4 == 0 && aligned(y, 4 * eb) && aligned(delta_log, 4 * eb);
     a.tiled_gqa = mapping == GDN_GQA_TILED;
     if ((B * Hv) > (int64_t)INT32_MAX / a.nchunks || (B * Hv) > (int64_t)INT32_MAX / a.row_blocks)
         return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large", fn);

@@ -56,7 +56,6 @@ constexpr int kCkRows = 16;        // state rows per scan CTA
 constexpr int kCkLocalThreads = 256;
 constexpr int kCkWsFloats = 2 * kCkC * kCkC + 2 * kCkC;  // Wb, Mq, Gam, aC per (b, hv, chunk)
 constexpr int kCkPartStride = 40;  // floats per row of a partial-product block (32 + pad)
-constexpr int kCkOutStride = 20;   // floats per step row of the y / delta staging tile
 
 __host__ __device__ constexpr int ck_kstride(int dk) { return dk + 8; }  // padded k / q row (elements)
 __host__ __device__ constexpr int ck_vstride(int esize) { return kCkRows + 16 / esize; }
@@ -66,9 +65,7 @@ __host__ __device__ constexpr size_t ck_slot_bytes(int dk, int esize) {
            align16((size_t)kCkC * ck_vstride(esize) * esize) + (size_t)kCkWsFloats * 4;
 }
 __host__ __device__ constexpr size_t chunk_scan_smem_bytes(int dk, int esize) {
-    return 3 * ck_slot_bytes(dk, esize) +
-           (size_t)2 * kCkWarps * kCkRows * kCkPartStride * 4 +
-           (size_t)2 * kCkC * kCkOutStride * 4;
+    return 3 * ck_slot_bytes(dk, esize) + (size_t)2 * kCkWarps * kCkRows * kCkPartStride * 4;
 }
 constexpr int kCkHeadsPerPass = 4;  // value heads of one key head processed side by side
 __host__ __device__ constexpr size_t chunk_local_smem_bytes(int dk) {
@@ -119,30 +116,6 @@ __device__ __forceinline__ float2 ld2f<__nv_bfloat16>(const __nv_bfloat16 *p) {
 template <>
 __device__ __forceinline__ float2 ld2f<__half>(const __half *p) {
     return __half22float2(*reinterpret_cast<const __half2 *>(p));
-}
-
-// Four consecutive values stored as T (16 bytes of f32, 8 of bf16 / f16).
-template <typename T>
-__device__ __forceinline__ void st4(T *p, float4 v);
-template <>
-__device__ __forceinline__ void st4<float>(float *p, float4 v) {
-    *reinterpret_cast<float4 *>(p) = v;
-}
-template <>
-__device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t *>(&a);
-    u.y = *reinterpret_cast<const uint32_t *>(&b);
-    *reinterpret_cast<uint2 *>(p) = u;
-}
-template <>
-__device__ __forceinline__ void st4<__half>(__half *p, float4 v) {
-    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t *>(&a);
-    u.y = *reinterpret_cast<const uint32_t *>(&b);
-    *reinterpret_cast<uint2 *>(p) = u;
 }
 
 // One 16-byte piece of T widened to f32 (exact).
@@ -366,7 +339,6 @@ chunk_scan_kernel(const ChunkArgs a) {
     constexpr int VS = ck_vstride(ES);
     constexpr int VVR = kCkRows / VEC;   // 16-byte pieces per staged v row
     constexpr int PS = kCkPartStride;
-    constexpr int OS = kCkOutStride;
     extern __shared__ __align__(16) unsigned char smem[];
 
     const int tid = threadIdx.x;
@@ -389,7 +361,6 @@ chunk_scan_kernel(const ChunkArgs a) {
     auto slotV = [&](int sl) { return reinterpret_cast<TIn *>(smem + sl * kSlot + kOffV); };
     auto slotW = [&](int sl) { return reinterpret_cast<float *>(smem + sl * kSlot + kOffW); };
     float *part = reinterpret_cast<float *>(smem + 3 * kSlot);         // [2][warps][16][PS]
-    float *otile = part + 2 * kCkWarps * kCkRows * PS;                 // [4 warps][8 steps][OS]
 
     const TIn *qp = static_cast<const TIn *>(a.q);
     const TIn *kp = static_cast<const TIn *>(a.k);
@@ -481,7 +452,6 @@ chunk_scan_kernel(const ChunkArgs a) {
     const int oh = warp & 1;  // this warp's n-tile: steps 8 oh .. 8 oh + 7
     const bool out_warp = ywarp || dp != nullptr;
     TIn *const outp = ywarp ? yp : dp;
-    float *const mytile = otile + warp * 8 * OS;
 
     int sl = 0, sl2 = 2;  // ring slots of chunks c and c + 2
     for (int64_t c = 0; c < nch; ++c) {
@@ -630,24 +600,14 @@ chunk_scan_kernel(const ChunkArgs a) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) o[e] = oh ? D[1][e] : D[0][e];
             }
-            // stage the 8 steps x 16 rows tile, then store whole step rows
+            // straight from the fragments: lane (g, t) holds rows g, g + 8 of
+            // steps 2t, 2t + 1, so each store writes four runs of 8 rows
 #pragma unroll
-            for (int e = 0; e < 4; ++e) mytile[(2 * t + (e & 1)) * OS + g + 8 * (e >> 1)] = o[e];
-            __syncwarp();
-            if (a.vec_out && vlim == kCkRows) {
-                const int sl8 = lane >> 2, x = 4 * (lane & 3), s = 8 * oh + sl8;
-                if (s < tcnt && ((bits >> s) & 1u))
-                    st4<TIn>(outp + ((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + x,
-                             *reinterpret_cast<const float4 *>(mytile + sl8 * OS + x));
-            } else {
-                for (int i = lane; i < 8 * kCkRows; i += 32) {
-                    const int sl8 = i / kCkRows, r = i - sl8 * kCkRows, s = 8 * oh + sl8;
-                    if (s < tcnt && ((bits >> s) & 1u) && r < vlim)
-                        outp[((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + r] =
-                            Elem<TIn>::from_f32(mytile[sl8 * OS + r]);
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int s = 8 * oh + 2 * t + (e & 1), r = g + 8 * (e >> 1);
+                if (s < tcnt && ((bits >> s) & 1u) && r < vlim)
+                    outp[((b * a.T + t0 + s) * a.Hv + hv) * a.Dv + row0 + r] = Elem<TIn>::from_f32(o[e]);
             }
-            __syncwarp();
         }
 
         // ---- S = Gam_{C-1} S + (D aC) K: B = raw k rows (k = step, n = column)

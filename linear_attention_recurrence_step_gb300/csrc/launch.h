@@ -74,7 +74,6 @@ struct ChunkArgs {
     int64_t nchunks;     // ceil(T / 16)
     int64_t row_blocks;  // ceil(Dv / 16)
     bool vec_v;          // v rows can be copied in 16-byte pieces
-    bool vec_out;        // y / delta_log rows can be stored four elements at a time
     bool tiled_gqa;      // key head hv % Hk instead of hv / (Hv/Hk)
 };
 
