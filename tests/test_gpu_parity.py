@@ -634,3 +634,48 @@ def test_state_in_t(dev, dtype, Dk, T):
                           workloads.widen(gl, dtype), s64, case.mask, accepted=acc.astype(np.int64))
     assert_close(to_host_f64(st2), want2, dtype, dtype, "per-sequence replay (state in T)")
     assert torch.equal(st2[0], s0[0])
+
+
+# ------------------------------------------------ CUDA graph capture
+@pytest.mark.parametrize("name", ["decode_b32_bf16", "rollback_b128_t16_bf16"])
+def test_cuda_graph_capture(dev, name):
+    """A serving loop captures the record + replay step in a CUDA graph and
+    replays it: every entry point used here is capturable (host checks,
+    launches on the capturing stream, nothing else), and the replayed graph
+    gives the eager results bit for bit."""
+    case = workloads.make_config(name, batch=8)
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    acc = case.accepted
+
+    def step(out):
+        gdn.gdn_step_record(q, k, v, g, beta, s0, mask, **out)
+        return gdn.gdn_state_replay(out["delta_log"], out["k_log"], out["g_log"], s0, mask,
+                                    accepted=acc)
+
+    eager_out = _alloc_outputs(case, dev)
+    eager_rep = step(eager_out)
+    torch.cuda.synchronize()
+
+    graph_out = _alloc_outputs(case, dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):  # warm-up on the side stream, as graph capture expects
+        step(graph_out)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    for t in graph_out.values():
+        t.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        graph_rep = step(graph_out)
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    for n in eager_out:
+        assert torch.equal(_bits(eager_out[n]), _bits(graph_out[n])), n
+    assert torch.equal(eager_rep, graph_rep)
+
+
+def _bits(x):
+    """The raw bits of a tensor (so NaN compares equal to the same NaN)."""
+    return x.view(torch.int16) if x.element_size() == 2 else x.view(torch.int32)
