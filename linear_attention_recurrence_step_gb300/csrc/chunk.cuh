@@ -27,8 +27,9 @@
 // Accuracy: every product runs as three tf32 MMAs (a_hi b_lo + a_lo b_hi +
 // a_hi b_hi, each operand split x = hi + lo with hi = x rounded to tf32 and
 // lo = x - hi exact in f32), about 21 significant bits per product with f32
-// accumulation; the state stays f32 in the accumulator fragments for the
-// whole launch.
+// accumulation; bf16 / f16 k and q are exact in tf32, so with those inputs
+// the products with a k / q operand take two.  The state stays f32 in the
+// accumulator fragments for the whole launch.
 //
 // Work split: a CTA owns 16 state rows of one (b, hv) tile and four warps
 // split the Dk columns (each holds 16 rows x Dk/4 of the state).  The partial
@@ -42,6 +43,8 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -331,6 +334,9 @@ __global__ void __launch_bounds__(kCkThreads)
 chunk_scan_kernel(const ChunkArgs a) {
     constexpr int C = kCkC;
     constexpr int KPW = DK / kCkWarps;   // state columns per warp
+    // bf16 / f16 values are exact in tf32: the low terms of k / q operands
+    // are zero, and their products are skipped
+    constexpr bool kTf32Exact = !std::is_same<TIn, float>::value;
     constexpr int NJ = KPW / 8;          // 8-column blocks per warp
     constexpr int KS = ck_kstride(DK);
     constexpr int ES = (int)sizeof(TIn);
@@ -482,7 +488,7 @@ chunk_scan_kernel(const ChunkArgs a) {
                 split_tf32(x.x, bh0, bl0);
                 split_tf32(x.y, bh1, bl1);
                 mma_tf32_1688(Pa[nt], al, bh0, bh1);
-                mma_tf32_1688(Pb[nt], ah, bl0, bl1);
+                if constexpr (!kTf32Exact) mma_tf32_1688(Pb[nt], ah, bl0, bl1);
                 mma_tf32_1688(Pm[nt], ah, bh0, bh1);
             }
         }
@@ -635,7 +641,7 @@ chunk_scan_kernel(const ChunkArgs a) {
                     split_tf32(Elem<TIn>::to_f32(cK[s0 * KS + col]), bh0, bl0);
                     split_tf32(Elem<TIn>::to_f32(cK[(s0 + 1) * KS + col]), bh1, bl1);
                     mma_tf32_1688(Ua[j], el[i], bh0, bh1);
-                    mma_tf32_1688(Ub[j], eh[i], bl0, bl1);
+                    if constexpr (!kTf32Exact) mma_tf32_1688(Ub[j], eh[i], bl0, bl1);
                     mma_tf32_1688(S[j], eh[i], bh0, bh1);
                 }
             }
