@@ -31,6 +31,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -195,6 +196,9 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
     constexpr int NCOL = tc_cols(DK);
     constexpr int DP = kTcRawPitch, KP = tc_kpitch(DK);
     constexpr int RD = tc_raw_depth(DK);
+    // bf16 / f16 k rows are exact in tf32: their low operand tile would be
+    // zero, so it is neither filled nor multiplied
+    constexpr bool kBExact = !std::is_same<TIn, float>::value;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *raw0 = smem + 2 * CANON;
     unsigned char *tail = raw0 + (STAGED ? RD * RAW : 0);
@@ -311,11 +315,15 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
         }
 #pragma unroll
         for (int j = 0; j < NB; ++j) {
-            float hi, lo;
-            tc_split(w0 != 0.f ? bv[j] : 0.f, hi, lo);
             const int off = ((2 * j + gq) * SBO + kq * 128 + cr * 16 + cs * 4) / 4;
-            Bh[off] = hi;
-            Bl[off] = lo;
+            if constexpr (kBExact) {
+                Bh[off] = w0 != 0.f ? bv[j] : 0.f;
+            } else {
+                float hi, lo;
+                tc_split(w0 != 0.f ? bv[j] : 0.f, hi, lo);
+                Bh[off] = hi;
+                Bl[off] = lo;
+            }
         }
         if (STAGED) cp_async_wait_group<RD - 2>();  // stage s+1 landed (this thread's pieces)
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -332,7 +340,8 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
                 const unsigned koff = k8 * 256;  // two core matrices along K per MMA
                 const uint32_t acc0 = (s > 0 || k8 > 0) ? 1u : 0u;
                 tc_mma_tf32(tmem, tc_desc(al + koff, 128, SBO), tc_desc(bh + koff, 128, SBO), idesc, acc0);
-                tc_mma_tf32(tmem, tc_desc(ah + koff, 128, SBO), tc_desc(bl + koff, 128, SBO), idesc, 1u);
+                if constexpr (!kBExact)
+                    tc_mma_tf32(tmem, tc_desc(ah + koff, 128, SBO), tc_desc(bl + koff, 128, SBO), idesc, 1u);
                 tc_mma_tf32(tmem, tc_desc(ah + koff, 128, SBO), tc_desc(bh + koff, 128, SBO), idesc, 1u);
             }
             tc_commit(smem_addr(&mbar_mma[s & 1]));
