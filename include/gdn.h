@@ -207,17 +207,31 @@ gdn_status gdn_chunk_prefill(const void *q, const void *k, const void *v,
 /*
  * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill without a caller workspace.
  *
- * The source pages have no counterpart to this entry point: it exists so a
- * caller that cannot provide device scratch memory can still run the chunked
- * prefill.  The workspace is a fixed 32 MiB block of device memory that the
- * library reserves for each device when its code loads (a static device
- * array; nothing is allocated per call).  Problems whose workspace
+ * The source pages have no counterpart to this entry point.  It is for
+ * callers that cannot allocate device memory when they call: an inference
+ * runtime that hands its whole HBM budget to its own pool allocator at start
+ * and forbids allocations afterwards, a plugin or script host that receives
+ * tensors but has no handle on the allocator that made them, or a serving
+ * loop with a latency budget in which cudaMalloc (which may synchronise the
+ * device) is not allowed.
+ *
+ * The workspace is a file-scope device array of 32 MiB inside the library (a
+ * static __device__ object): every GPU on which the library's device code is
+ * loaded holds those 32 MiB until the process exits, and no call allocates,
+ * frees or synchronises anything.  Each call looks up the array's device
+ * address for the current device (cudaGetSymbolAddress); the first call on a
+ * device may also load the library's device code there, so make that first
+ * call before any stream capture begins.  Problems whose workspace
  * (gdn_chunk_prefill_workspace_size) exceeds 32 MiB return
- * GDN_ERR_UNSUPPORTED before anything is launched.  All calls on one device
- * share the block, so they must not overlap in time (issue them on one
- * stream, or use gdn_chunk_prefill with a workspace per stream).  Results
- * are identical, bit for bit, to gdn_chunk_prefill with the same arguments;
- * every other argument, rule and error is as documented there.
+ * GDN_ERR_UNSUPPORTED before anything is launched.
+ *
+ * All calls on one device share the array, and each call leaves its contents
+ * behind; a call writes every workspace entry it reads before reading it, so
+ * nothing needs clearing between calls.  Calls whose kernels overlap in time
+ * on one device race on the array and give wrong results: issue them on one
+ * stream (or use gdn_chunk_prefill with a workspace per stream).  Results are
+ * identical, bit for bit, to gdn_chunk_prefill with the same arguments; every
+ * other argument, rule and error is as documented there.
  */
 gdn_status gdn_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
                                      const void *g, const void *beta,

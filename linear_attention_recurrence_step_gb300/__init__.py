@@ -308,8 +308,10 @@ def gdn_chunk_prefill(q, k, v, g, beta, state_in, mask=None, *, y=None, state_ou
 
 
 def gdn_chunk_prefill_noalloc(q, k, v, g, beta, state_in, mask=None, **kw) -> RecordOutputs:
-    """``gdn_chunk_prefill`` on the library's static 32 MiB scratch (no
-    workspace argument; calls on one device must not overlap in time)."""
+    """``gdn_chunk_prefill`` on the library's static 32 MiB device scratch, for
+    callers that may not allocate device memory when they call (no workspace
+    argument; calls on one device share the scratch and must not overlap in
+    time)."""
     return gdn_chunk_prefill(q, k, v, g, beta, state_in, mask, workspace="static", **kw)
 
 

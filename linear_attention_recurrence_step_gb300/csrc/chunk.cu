@@ -1,7 +1,5 @@
 // chunk.cu -- launches of the chunked-prefill kernels (chunk.cuh) for every
 // element type and compiled Dk.
-#include <mutex>
-
 #include "chunk.cuh"
 
 namespace gdn {
@@ -20,22 +18,16 @@ cudaError_t launch_chunk(DType dt, int dk, const ChunkArgs &a, cudaStream_t s) {
 // call time).  Calls that use it must not overlap in time on one device.
 static __device__ __align__(256) float g_chunk_scratch[kChunkStaticScratchBytes / sizeof(float)];
 
+// The address of a __device__ symbol belongs to the CUDA context that loaded
+// the module, not to the device index: after cudaDeviceReset, or when a
+// driver-API caller makes another context current on the same device, an
+// address remembered from an earlier call would be stale.  So the address is
+// looked up on every call (cheap next to the two launches that use it).
 cudaError_t chunk_static_scratch(float **ptr) {
-    constexpr int kMaxDevices = 64;
-    static float *addr[kMaxDevices] = {};
-    static std::mutex lock;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_chunk_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> guard(lock);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_chunk_scratch);
-        if (e != cudaSuccess) return e;
-        addr[dev] = static_cast<float *>(p);
-    }
-    *ptr = addr[dev];
+    *ptr = static_cast<float *>(p);
     return cudaSuccess;
 }
 

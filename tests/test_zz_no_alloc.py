@@ -1,11 +1,18 @@
 """gdn_chunk_prefill_noalloc: the chunked prefill on the library's static
-device scratch (no caller workspace).  The source pages have no counterpart
-to this entry point.
+device scratch, for callers that cannot allocate device memory when they
+call (a runtime whose pool allocator owns all of HBM, a plugin host without
+access to the allocator, a serving loop that may not call cudaMalloc).  The
+source pages have no counterpart to this entry point.
 
-* parity with the float64 oracle and bit-equality with gdn_chunk_prefill on
-  a caller workspace (same kernels, same arithmetic);
+* two calls in a row on different inputs, each bit-equal to
+  gdn_chunk_prefill on a caller workspace (same kernels, same arithmetic):
+  the second call must not see what the first left in the shared scratch;
+* parity with the float64 oracle;
 * a problem whose workspace exceeds the 32 MiB static block is refused with
   GDN_ERR_UNSUPPORTED before anything is launched.
+
+This file is collected last, so a run that stops at the first failure has
+already run every other test; it also passes alone in a fresh process.
 """
 from __future__ import annotations
 
@@ -32,9 +39,7 @@ def dev():
     return torch.device("cuda:0")
 
 
-def test_noalloc_matches_workspace_call_and_oracle(dev):
-    case = workloads.make_case(B=2, T=77, Hk=2, Hv=4, Dk=128, Dv=48, dtype="f32", seed=801,
-                               mask="bernoulli:0.8")
+def _call_pair(case, dev):
     q, k, v, g, beta, s0, mask = device_inputs(case, dev)
     a = gdn.gdn_chunk_prefill_noalloc(q, k, v, g, beta, s0, mask, gqa="tiled", capture_tape=True)
     b = gdn.gdn_chunk_prefill(q, k, v, g, beta, s0, mask, gqa="tiled", capture_tape=True)
@@ -42,11 +47,24 @@ def test_noalloc_matches_workspace_call_and_oracle(dev):
     on = torch.from_numpy(case.mask.astype(bool)).to(dev)
     assert torch.equal(a.state_out, b.state_out)
     assert torch.equal(a.y[on], b.y[on]) and torch.equal(a.delta_log[on], b.delta_log[on])
-    ref = oracle.record(case.f64("q"), case.f64("k"), case.f64("v"), case.f64("g"),
-                        case.f64("beta"), case.f64("state"), case.mask, gqa="tiled")
-    act = case.mask.astype(bool)
-    assert_close(to_host_f64(a.state_out), ref["state_out"], "f32", None, "state_out")
-    assert_close(to_host_f64(a.y)[act], ref["y"][act], "f32", None, "y")
+    return a
+
+
+def test_noalloc_two_calls_match_workspace_call_and_oracle(dev):
+    # two calls in a row on different problems (the second smaller, so every
+    # scratch block it uses still holds the first call's data when it
+    # starts): both must equal the workspace entry point bit for bit
+    first = workloads.make_case(B=2, T=77, Hk=2, Hv=4, Dk=128, Dv=48, dtype="f32", seed=801,
+                                mask="bernoulli:0.8")
+    second = workloads.make_case(B=1, T=40, Hk=2, Hv=4, Dk=128, Dv=48, dtype="f32", seed=802,
+                                 mask="bernoulli:0.8")
+    for case in (first, second):
+        a = _call_pair(case, dev)
+        ref = oracle.record(case.f64("q"), case.f64("k"), case.f64("v"), case.f64("g"),
+                            case.f64("beta"), case.f64("state"), case.mask, gqa="tiled")
+        act = case.mask.astype(bool)
+        assert_close(to_host_f64(a.state_out), ref["state_out"], "f32", None, "state_out")
+        assert_close(to_host_f64(a.y)[act], ref["y"][act], "f32", None, "y")
 
 
 def test_noalloc_long_prefill_fits(dev):
