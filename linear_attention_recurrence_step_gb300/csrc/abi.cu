@@ -233,10 +233,14 @@ gdn_status record_impl(const char *fn, const void *q, const void *k, const void 
                       aligned(v, 16) && (Dv * eb) % 16 == 0, mapping == GDN_GQA_TILED,
                       tstate && dtype != GDN_DTYPE_F32};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    switch (dtype) {
-    case GDN_DTYPE_F32: e = gdn::launch_record_f32((int)Dk, a, geo, s); break;
-    case GDN_DTYPE_BF16: e = gdn::launch_record_bf16((int)Dk, a, geo, s); break;
-    case GDN_DTYPE_F16: e = gdn::launch_record_f16((int)Dk, a, geo, s); break;
+    if (geo.mma && gdn::record_tc_eligible(a, (int)Dk, dtype == GDN_DTYPE_BF16)) {
+        e = gdn::launch_record_tc(a, sms, s);  // one chunk on tcgen05, the TMA-fed stream
+    } else {
+        switch (dtype) {
+        case GDN_DTYPE_F32: e = gdn::launch_record_f32((int)Dk, a, geo, s); break;
+        case GDN_DTYPE_BF16: e = gdn::launch_record_bf16((int)Dk, a, geo, s); break;
+        case GDN_DTYPE_F16: e = gdn::launch_record_f16((int)Dk, a, geo, s); break;
+        }
     }
     if (e != cudaSuccess) return cuda_fail(fn, "launch", e);
     return ok();

@@ -116,6 +116,12 @@ Geometry replay_geometry(int dk, int64_t tiles, int64_t Dv, int64_t steps, int e
 cudaError_t launch_record_f32(int dk, const RecordArgs &a, const Geometry &geo, cudaStream_t s);
 cudaError_t launch_record_bf16(int dk, const RecordArgs &a, const Geometry &geo, cudaStream_t s);
 cudaError_t launch_record_f16(int dk, const RecordArgs &a, const Geometry &geo, cudaStream_t s);
+// The tcgen05 record kernel (record_tc.cuh): bf16 calls of at most 16 steps,
+// f32 state, Dk = 128, Dv a multiple of 128; its wait-expiry flag (device
+// address).
+bool record_tc_eligible(const RecordArgs &a, int dk, bool bf16);
+cudaError_t launch_record_tc(const RecordArgs &a, int sm_count, cudaStream_t s);
+cudaError_t record_tc_wait_flag(unsigned **ptr);
 cudaError_t launch_replay(DType dt, int dk, const ReplayArgs &a, const Geometry &geo,
                           cudaStream_t s);
 cudaError_t launch_repeat(const RepeatArgs &a, cudaStream_t s, int sm_count);

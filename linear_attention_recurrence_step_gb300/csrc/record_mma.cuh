@@ -96,6 +96,18 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *row) {
                  : "r"(a));
 }
 
+// The same, from a shared-memory address.
+__device__ __forceinline__ void ldsm_x4_a(uint32_t (&r)[4], uint32_t a) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t_a(uint32_t (&r)[4], uint32_t a) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+
 // (x0, x1) ~ hi + lo with hi, lo packed bf16 pairs (x0 in the low half).
 // x - bf16(x) is exact in f32, so the pair carries 16 significant bits.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
