@@ -60,7 +60,7 @@ namespace gdn {
 constexpr int kRtRows = 128;       // state rows per unit (tensor-memory lanes)
 constexpr int kRtDk = 128;         // key dimension of this kernel
 constexpr int kRtGroups = 2;       // warpgroups (units in flight) per CTA
-constexpr int kRtThreads = 160 * kRtGroups;  // per warpgroup: four row warps + a preparation warp
+constexpr int kRtThreads = 192 * kRtGroups;  // per warpgroup: four row warps, a preparation warp, an issuer warp
 constexpr uint32_t kRtTmemCols = 512;   // S (128) + P (32) per warpgroup, 256 apart
 constexpr long long kRtWaitCycles = 2000000000ll;  // bound on any mbarrier wait (~1 s)
 
@@ -79,9 +79,12 @@ constexpr uint32_t kRtOffA2 = kRtOffV + 2 * kRtV;
 constexpr uint32_t kRtOffB2 = kRtOffA2 + kRtA2;
 constexpr uint32_t kRtOffPrep = kRtOffB2 + kRtB2;
 constexpr uint32_t kRtGroupBytes = kRtOffPrep + 2 * kRtPrepAl;
-// mbarriers per warpgroup: state landed, inputs landed [2], MMA1 done, MMA2
-// done, preparation ready [2], unit finished [2] (one spare)
-constexpr int kRtBars = 10;
+// mbarriers per warpgroup: 0 state landed, 1-2 inputs landed [buf], 3 MMA1
+// done, 4 MMA2 done, 5-6 preparation ready [buf], 7-8 unit finished [buf],
+// 9 operand tiles written (pass), 10 d tiles written (solve); one spare
+constexpr int kRtBars = 12;
+constexpr int kRtBarState = 0, kRtBarIn = 1, kRtBarMma1 = 3, kRtBarMma2 = 4, kRtBarPrep = 5,
+              kRtBarDone = 7, kRtBarPass = 9, kRtBarSolve = 10;
 constexpr uint32_t kRtSmem = kRtGroups * kRtGroupBytes + kRtGroups * kRtBars * 8 + 16 + 1024;
 static_assert(kRtPrep <= kRtPrepAl, "preparation block");
 static_assert(kRtGroupBytes % 1024 == 0, "warpgroup region alignment");
@@ -147,6 +150,12 @@ __device__ __forceinline__ void rt_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// 16 lanes x 256 bits, sixteen 8-column blocks (the layout of rt_ld16x256_x4).
+__device__ __forceinline__ void rt_ld16x256_x16(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+                 : "r"(taddr));
+}
 __device__ __forceinline__ void rt_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -187,12 +196,14 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
     auto gptr = [&](uint32_t s) { return gbase + (s - base); };  // generic pointer of a shared address
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool prep_warp = warp >= 4 * kRtGroups;
-    const int wg = prep_warp ? warp - 4 * kRtGroups : warp >> 2;  // the warpgroup served
+    // warps 0-3 / 4-7: the row warps of warpgroups 0 / 1; then one preparation
+    // warp and one issuer warp per warpgroup
+    const bool prep_warp = warp >= 4 * kRtGroups && warp < 5 * kRtGroups;
+    const bool issuer_warp = warp >= 5 * kRtGroups;
+    const int wg = issuer_warp ? warp - 5 * kRtGroups : prep_warp ? warp - 4 * kRtGroups : warp >> 2;
     const int r = tid & 127;  // state row / tensor-memory lane of this thread in its unit
     const uint32_t barbase = base + kRtGroups * kRtGroupBytes;
     auto bar = [&](int g, int i) { return barbase + (uint32_t)(g * kRtBars + i) * 8u; };
-    // per warpgroup: 0 sfull, 1-2 infull[buf], 3 mma1, 4 mma2, 5-6 prepdone[buf], 7-8 unitdone[buf]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gptr(barbase + kRtGroups * kRtBars * 8));
 
     const int tcnt = (int)a.T;  // <= C
@@ -222,7 +233,13 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     if (tid == 0) {
-        for (int i = 0; i < kRtGroups * kRtBars; ++i) mbar_init(barbase + 8u * i, 1);
+        for (int g = 0; g < kRtGroups; ++g)
+            for (int i = 0; i < kRtBars; ++i) {
+                // arrivals: one from the thread that issues (or prepares), or one
+                // per row warp
+                const bool per_warp = i == kRtBarDone || i == kRtBarDone + 1 || i == kRtBarPass || i == kRtBarSolve;
+                mbar_init(bar(g, i), per_warp ? 4u : 1u);
+            }
         mbar_init_fence();
     }
     rt_fence_before();
@@ -265,8 +282,8 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
             const Unit dn = unit_of(g, j + 1);
             prefetch(dn);
             // this buffer's previous unit (j - 2) is finished; the k / q rows landed
-            if (j >= 2) ok = mbar_wait_bounded(bar(g, 7 + buf), (uint32_t)(((j >> 1) - 1) & 1), kRtWaitCycles);
-            ok = ok && mbar_wait_bounded(bar(g, 1 + buf), (uint32_t)((j >> 1) & 1), kRtWaitCycles);
+            if (j >= 2) ok = mbar_wait_bounded(bar(g, kRtBarDone + buf), (uint32_t)(((j >> 1) - 1) & 1), kRtWaitCycles);
+            ok = ok && mbar_wait_bounded(bar(g, kRtBarIn + buf), (uint32_t)((j >> 1) & 1), kRtWaitCycles);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             // Gram matrices KK[u][s] = k_u . k_s and KQ[u][s] = k_u . q_s (mma.sync)
@@ -345,73 +362,137 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                 if (glp && lin && ((bits >> lane) & 1u)) st_from_f32(glp + (bt0 + lane) * a.Hv + d.hv, gv);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(g, 5 + buf));  // the unit's preparation block is ready
+            if (lane == 0) mbar_arrive(bar(g, kRtBarPrep + buf));  // the unit's preparation block is ready
             d = dn;
         }
         if (!ok && lane == 0) atomicExch(ta.wait_flag, 1u);
-    } else {
-        // ================================================ a warpgroup
+    } else if (issuer_warp) {
+        // ================================================ issuer warp (lane 0)
+        // TMA loads of the warpgroup's units and its tcgen05.mma products
         const uint32_t gb = base + (uint32_t)wg * kRtGroupBytes;
         const uint32_t slot = gb;
-        const uint32_t tm_s = tmem0 + (uint32_t)(wg * 256);   // S: columns [0, 128)
-        const uint32_t tm_p = tm_s + 128;                     // P: columns [128, 160)
+        const uint32_t tm_s = tmem0 + (uint32_t)(wg * 256);  // S: columns [0, 128)
+        const uint32_t tm_p = tm_s + 128;                    // P: columns [128, 160)
+        if (lane == 0) {
+            const uint64_t pol_state = l2_evict_first_policy();
+            auto issue_state = [&](const Unit &d) {
+                mbar_arrive_expect_tx(bar(wg, kRtBarState), kRtSlot);
+#pragma unroll
+                for (int bx = 0; bx < kRtDk / 32; ++bx)
+                    tma_load_3d(slot + bx * 16384, &tm_state, bx * 32, (int)d.row0, (int)d.n, bar(wg, kRtBarState),
+                                pol_state);
+            };
+            auto issue_in = [&](const Unit &d, int buf) {
+                const uint32_t kq = gb + kRtOffKq + buf * kRtKq, vb = gb + kRtOffV + buf * kRtV;
+                const uint32_t bb = bar(wg, kRtBarIn + buf);
+                mbar_arrive_expect_tx(bb, kRtKq + kRtV);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    tma_load_4d(kq + h * 4096, &tm_k, h * 64, (int)d.hk, 0, (int)d.b, bb);
+                    tma_load_4d(kq + h * 4096 + 2048, &tm_q, h * 64, (int)d.hk, 0, (int)d.b, bb);
+                }
+                tma_load_4d(vb, &tm_v, (int)d.row0, (int)d.hv, 0, (int)d.b, bb);
+            };
+            const uint32_t id1 = rt_idesc_bf16(2 * C), id2 = rt_idesc_bf16(kRtDk);
+            // the last unit whose copies / products were issued, to drain them if
+            // a wait runs out
+            int64_t last_s = -1, last_in[2] = {-1, -1}, last_m1 = -1, last_m2 = -1;
+            bool ok = true;
+            Unit d = unit_of(wg, 0);
+            if (d.valid) {
+                issue_state(d);
+                issue_in(d, 0);
+                last_s = 0;
+                last_in[0] = 0;
+            }
+            for (int64_t j = 0; ok && d.valid; ++j) {
+                const int buf = (int)(j & 1);
+                const uint32_t kq = gb + kRtOffKq + buf * kRtKq;
+                const Unit dn = unit_of(wg, j + 1);
+                if (dn.valid) {  // the next unit's inputs, once their buffer's last unit (j - 1) is done
+                    if (j >= 1)
+                        ok = mbar_wait_bounded(bar(wg, kRtBarDone + (buf ^ 1)), (uint32_t)(((j - 1) >> 1) & 1),
+                                               kRtWaitCycles);
+                    if (!ok) break;
+                    issue_in(dn, buf ^ 1);
+                    last_in[buf ^ 1] = j + 1;
+                }
+                // MMA1: P = [S hi; S lo] [K; Q]^T, once the row warps wrote the operand tiles
+                ok = mbar_wait_bounded(bar(wg, kRtBarPass), (uint32_t)(j & 1), kRtWaitCycles) &&
+                     mbar_wait_bounded(bar(wg, kRtBarIn + buf), (uint32_t)((j >> 1) & 1), kRtWaitCycles);
+                if (!ok) break;
+                rt_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kRtDk / 16; ++kk) {
+                    const uint32_t abase = slot + (uint32_t)(kk >> 1) * 16384u + (uint32_t)(kk & 1) * 32u;
+                    const uint64_t db =
+                        rt_desc(kq + (uint32_t)(kk >> 2) * 4096u + (uint32_t)(kk & 3) * 32u, 16, 1024, 2);
+                    rt_mma(tm_p, rt_desc(abase, 16, 512, 4), db, id1, kk > 0 ? 1u : 0u);
+                    rt_mma(tm_p, rt_desc(abase + 8192u, 16, 512, 4), db, id1, 1u);
+                }
+                rt_commit(bar(wg, kRtBarMma1));
+                last_m1 = j;
+                // the slot is free once MMA1 has read it: the next unit's state rows
+                ok = mbar_wait_bounded(bar(wg, kRtBarMma1), (uint32_t)(j & 1), kRtWaitCycles);
+                if (!ok) break;
+                if (dn.valid) {
+                    issue_state(dn);
+                    last_s = j + 1;
+                }
+                // MMA2: S += [D hi; D lo] K, once the row warps wrote D and K^T
+                ok = mbar_wait_bounded(bar(wg, kRtBarSolve), (uint32_t)(j & 1), kRtWaitCycles);
+                if (!ok) break;
+                rt_fence_after();
+                const uint64_t db = rt_desc(gb + kRtOffB2, 128, 256, 0);
+                rt_mma(tm_s, rt_desc(gb + kRtOffA2, 128, 256, 0), db, id2, 1u);
+                rt_mma(tm_s, rt_desc(gb + kRtOffA2 + 4096u, 128, 256, 0), db, id2, 1u);
+                rt_commit(bar(wg, kRtBarMma2));
+                last_m2 = j;
+                d = dn;
+            }
+            if (!ok) {
+                atomicExch(ta.wait_flag, 1u);
+                // let every copy and product this warp issued land before the CTA
+                // releases its shared and tensor memory (bounded again)
+                if (last_s >= 0) mbar_wait_bounded(bar(wg, kRtBarState), (uint32_t)(last_s & 1), kRtWaitCycles);
+                for (int b2 = 0; b2 < 2; ++b2)
+                    if (last_in[b2] >= 0)
+                        mbar_wait_bounded(bar(wg, kRtBarIn + b2), (uint32_t)((last_in[b2] >> 1) & 1), kRtWaitCycles);
+                if (last_m1 >= 0) mbar_wait_bounded(bar(wg, kRtBarMma1), (uint32_t)(last_m1 & 1), kRtWaitCycles);
+                if (last_m2 >= 0) mbar_wait_bounded(bar(wg, kRtBarMma2), (uint32_t)(last_m2 & 1), kRtWaitCycles);
+            }
+        }
+    } else {
+        // ================================================ the row warps of a warpgroup
+        const uint32_t gb = base + (uint32_t)wg * kRtGroupBytes;
+        const uint32_t slot = gb;
+        const uint32_t tm_s = tmem0 + (uint32_t)(wg * 256);  // S: columns [0, 128)
+        const uint32_t tm_p = tm_s + 128;                    // P: columns [128, 160)
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        const bool issuer = r == 0;
         const int barid = 1 + wg;
-        const uint64_t pol_state = l2_evict_first_policy();
         T *yp = static_cast<T *>(a.y);
         T *dp = static_cast<T *>(a.delta_log);
         float *sout = static_cast<float *>(a.state_out);
-
-        auto issue_state = [&](const Unit &d) {
-            mbar_arrive_expect_tx(bar(wg, 0), kRtSlot);
-#pragma unroll
-            for (int bx = 0; bx < kRtDk / 32; ++bx)
-                tma_load_3d(slot + bx * 16384, &tm_state, bx * 32, (int)d.row0, (int)d.n, bar(wg, 0), pol_state);
-        };
-        auto issue_in = [&](const Unit &d, int buf) {
-            const uint32_t kq = gb + kRtOffKq + buf * kRtKq, vb = gb + kRtOffV + buf * kRtV;
-            const uint32_t bb = bar(wg, 1 + buf);
-            mbar_arrive_expect_tx(bb, kRtKq + kRtV);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                tma_load_4d(kq + h * 4096, &tm_k, h * 64, (int)d.hk, 0, (int)d.b, bb);
-                tma_load_4d(kq + h * 4096 + 2048, &tm_q, h * 64, (int)d.hk, 0, (int)d.b, bb);
+        // a wait that runs out raises the flag at once; the warpgroup stops at
+        // its next shared barrier
+        auto wait = [&](uint32_t b, int64_t phase, bool &okv) {
+            if (okv && !mbar_wait_bounded(b, (uint32_t)(phase & 1), kRtWaitCycles)) {
+                okv = false;
+                atomicExch(ta.wait_flag, 1u);
             }
-            tma_load_4d(vb, &tm_v, (int)d.row0, (int)d.hv, 0, (int)d.b, bb);
         };
-
-        // the last unit index whose copies / products were issued (issuer's
-        // bookkeeping, to drain them if a wait runs out)
-        int64_t last_s = -1, last_in[2] = {-1, -1}, last_m1 = -1, last_m2 = -1;
-        Unit cur = unit_of(wg, 0);
-        if (issuer && cur.valid) {
-            issue_state(cur);
-            issue_in(cur, 0);
-            last_s = 0;
-            last_in[0] = 0;
-        }
-        const uint32_t id1 = rt_idesc_bf16(2 * C), id2 = rt_idesc_bf16(kRtDk);
         bool ok = true;
-        int64_t j = 0;
-        for (;; ++j) {
-            if (!cur.valid) break;
-            const Unit d = cur;
+        for (int64_t j = 0;; ++j) {
+            const Unit d = unit_of(wg, j);
+            if (!d.valid) break;
             const int buf = (int)(j & 1);
             const uint32_t kq = gb + kRtOffKq + buf * kRtKq;
             const T *vs = reinterpret_cast<const T *>(gptr(gb + kRtOffV + buf * kRtV));
             const RtPrep *pp = reinterpret_cast<const RtPrep *>(gptr(gb + kRtOffPrep + buf * kRtPrepAl));
-            const Unit nx = unit_of(wg, j + 1);
-            if (issuer && nx.valid) {
-                issue_in(nx, buf ^ 1);  // its buffer's last unit (j - 1) is done
-                last_in[buf ^ 1] = j + 1;
-            }
 
             // ---- the state rows: into S (tensor memory) and, in place, into the
             // bf16 hi / lo operand tiles of MMA1 (two boxes of 32 columns at a time)
-            ok = mbar_wait_bounded(bar(wg, 0), (uint32_t)(j & 1), kRtWaitCycles);
-            ok = named_bar_or(barid, 128, !ok) ? false : true;
-            if (!ok) break;
+            wait(bar(wg, kRtBarState), j, ok);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t x[2][32];
@@ -429,7 +510,16 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                     }
                     rt_st32(tm_s + lane_off + (uint32_t)(32 * bx), x[bb2]);
                 }
-                named_bar_sync(barid, 128);  // both boxes read by every row before they are rewritten
+                // both boxes read by every row before they are rewritten; the
+                // first of these barriers also stops the warpgroup after a failed wait
+                if (half == 0) {
+                    if (named_bar_or(barid, 128, !ok)) {
+                        ok = false;
+                        break;
+                    }
+                } else {
+                    named_bar_sync(barid, 128);
+                }
 #pragma unroll
                 for (int bb2 = 0; bb2 < 2; ++bb2) {
                     const int bx = 2 * half + bb2;
@@ -448,43 +538,37 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                     }
                 }
             }
+            if (!ok) {
+                // poison this unit's state rows
+                float *orow = sout + ((int64_t)d.n * a.Dv + d.row0 + r) * kRtDk;
+                const float nan = __int_as_float(0x7fc00000);
+                for (int c = 0; c < kRtDk / 4; ++c)
+                    __stcs(reinterpret_cast<float4 *>(orow) + c, make_float4(nan, nan, nan, nan));
+                break;
+            }
             rt_wait_st();
             fence_async_smem();
             rt_fence_before();
-            ok = mbar_wait_bounded(bar(wg, 1 + buf), (uint32_t)((j >> 1) & 1), kRtWaitCycles);  // k / q / v
-            ok = named_bar_or(barid, 128, !ok) ? false : true;
-            if (!ok) break;
-
-            // ---- MMA1: P = [S hi; S lo] [K; Q]^T
-            if (issuer) {
-                rt_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kRtDk / 16; ++kk) {
-                    const uint32_t abase = slot + (uint32_t)(kk >> 1) * 16384u + (uint32_t)(kk & 1) * 32u;
-                    const uint64_t db = rt_desc(kq + (uint32_t)(kk >> 2) * 4096u + (uint32_t)(kk & 3) * 32u, 16, 1024, 2);
-                    rt_mma(tm_p, rt_desc(abase, 16, 512, 4), db, id1, kk > 0 ? 1u : 0u);
-                    rt_mma(tm_p, rt_desc(abase + 8192u, 16, 512, 4), db, id1, 1u);
-                }
-                rt_commit(bar(wg, 3));
-                last_m1 = j;
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(wg, kRtBarPass));
 
             // ---- while MMA1 runs: the step scalars, K^T (inactive steps zero)
             // and this row's v entries
-            ok = mbar_wait_bounded(bar(wg, 5 + buf), (uint32_t)((j >> 1) & 1), kRtWaitCycles);
-            ok = __all_sync(0xffffffffu, ok);
+            wait(bar(wg, kRtBarPrep + buf), j >> 1, ok);
+            wait(bar(wg, kRtBarIn + buf), j >> 1, ok);
             const unsigned bits = pp->bits;
             {
                 // thread r writes column n = r of K^T: 16 steps, two 8-step core-matrix columns
                 uint32_t w2[8];
 #pragma unroll
-                for (int s = 0; s < C; s += 2) {
-                    const uint32_t a0 = rt_kq_addr(kq, false, s, r & ~7) + (uint32_t)(r & 7) * 2u;
-                    const uint32_t a1 = rt_kq_addr(kq, false, s + 1, r & ~7) + (uint32_t)(r & 7) * 2u;
-                    const uint32_t lo16 = ((bits >> s) & 1u) ? *reinterpret_cast<const unsigned short *>(gptr(a0)) : 0u;
+                for (int s2 = 0; s2 < C; s2 += 2) {
+                    const uint32_t a0 = rt_kq_addr(kq, false, s2, r & ~7) + (uint32_t)(r & 7) * 2u;
+                    const uint32_t a1 = rt_kq_addr(kq, false, s2 + 1, r & ~7) + (uint32_t)(r & 7) * 2u;
+                    const uint32_t lo16 =
+                        ((bits >> s2) & 1u) ? *reinterpret_cast<const unsigned short *>(gptr(a0)) : 0u;
                     const uint32_t hi16 =
-                        ((bits >> (s + 1)) & 1u) ? *reinterpret_cast<const unsigned short *>(gptr(a1)) : 0u;
-                    w2[s >> 1] = lo16 | (hi16 << 16);
+                        ((bits >> (s2 + 1)) & 1u) ? *reinterpret_cast<const unsigned short *>(gptr(a1)) : 0u;
+                    w2[s2 >> 1] = lo16 | (hi16 << 16);
                 }
                 unsigned char *b2 = gptr(gb + kRtOffB2 + (uint32_t)(r >> 3) * 256u + (uint32_t)(r & 7) * 16u);
                 *reinterpret_cast<uint4 *>(b2) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
@@ -492,16 +576,10 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
             }
             float vv[C];
 #pragma unroll
-            for (int s = 0; s < C; ++s) vv[s] = __bfloat162float(vs[s * kRtRows + r]);
+            for (int s2 = 0; s2 < C; ++s2) vv[s2] = __bfloat162float(vs[s2 * kRtRows + r]);
 
-            ok = ok && mbar_wait_bounded(bar(wg, 3), (uint32_t)(j & 1), kRtWaitCycles);
-            ok = __all_sync(0xffffffffu, ok);
+            wait(bar(wg, kRtBarMma1), j, ok);
             rt_fence_after();
-            // the slot is free: the next unit's state rows
-            if (issuer && nx.valid && ok) {
-                issue_state(nx);
-                last_s = j + 1;
-            }
 
             // ---- this row's step dots, and the FP32 solve
             uint32_t pr[32];
@@ -618,27 +696,15 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
             }
             fence_async_smem();
             rt_fence_before();
-            ok = !named_bar_or(barid, 128, !ok);
-            if (!ok) break;
-
-            // ---- MMA2: S += [D hi; D lo] K
-            if (issuer) {
-                rt_fence_after();
-                const uint64_t db = rt_desc(gb + kRtOffB2, 128, 256, 0);
-                rt_mma(tm_s, rt_desc(gb + kRtOffA2, 128, 256, 0), db, id2, 1u);
-                rt_mma(tm_s, rt_desc(gb + kRtOffA2 + 4096u, 128, 256, 0), db, id2, 1u);
-                rt_commit(bar(wg, 4));
-                last_m2 = j;
-            }
-            ok = mbar_wait_bounded(bar(wg, 4), (uint32_t)(j & 1), kRtWaitCycles);
-            ok = __all_sync(0xffffffffu, ok);
-            rt_fence_after();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(wg, kRtBarSolve));
 
             // ---- s = G s^, streaming stores.  The accumulator is read in the
-            // m16n8 fragment shape (16x256b): per load, thread t holds rows
-            // t/4 and 8 + t/4 of a 16-lane half and columns 2(t%4), 2(t%4)+1 of
-            // each 8-column block, so every store instruction writes 8 rows x
-            // 32 contiguous bytes.
+            // m16n8 fragment shape (16x256b): thread t holds rows t/4 and 8 + t/4
+            // of a 16-lane half and columns 2(t%4), 2(t%4)+1 of every 8-column
+            // block, so every store instruction writes 8 rows x 32 contiguous bytes.
+            wait(bar(wg, kRtBarMma2), j, ok);
+            rt_fence_after();
             const float Gf = pp->gfinal;
             const int q = warp & 3;
 #pragma unroll 1
@@ -646,46 +712,20 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                 const int rbase = 32 * q + 16 * h + (lane >> 2);
                 float *o0 = sout + ((int64_t)d.n * a.Dv + d.row0 + rbase) * kRtDk + 2 * (lane & 3);
                 float *o1 = o0 + 8 * kRtDk;
-#pragma unroll 1
-                for (int c = 0; c < kRtDk / 32; ++c) {
-                    uint32_t sv[16];
-                    rt_ld16x256_x4(tm_s + ((uint32_t)(32 * q + 16 * h) << 16) + (uint32_t)(32 * c), sv);
-                    rt_wait_ld();
+                uint32_t sv[64];
+                rt_ld16x256_x16(tm_s + ((uint32_t)(32 * q + 16 * h) << 16), sv);
+                rt_wait_ld();
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        __stcs(reinterpret_cast<float2 *>(o0 + 32 * c + 8 * m),
-                               make_float2(__uint_as_float(sv[4 * m]) * Gf, __uint_as_float(sv[4 * m + 1]) * Gf));
-                        __stcs(reinterpret_cast<float2 *>(o1 + 32 * c + 8 * m),
-                               make_float2(__uint_as_float(sv[4 * m + 2]) * Gf, __uint_as_float(sv[4 * m + 3]) * Gf));
-                    }
+                for (int m = 0; m < 16; ++m) {
+                    __stcs(reinterpret_cast<float2 *>(o0 + 8 * m),
+                           make_float2(__uint_as_float(sv[4 * m]) * Gf, __uint_as_float(sv[4 * m + 1]) * Gf));
+                    __stcs(reinterpret_cast<float2 *>(o1 + 8 * m),
+                           make_float2(__uint_as_float(sv[4 * m + 2]) * Gf, __uint_as_float(sv[4 * m + 3]) * Gf));
                 }
             }
             rt_fence_before();
-            ok = !named_bar_or(barid, 128, !ok);  // the unit's buffers and tensor memory are free
-            if (!ok) break;
-            if (issuer) mbar_arrive(bar(wg, 7 + buf));
-            cur = nx;
-        }
-        if (!ok) {
-            // a wait ran out: poison this unit's state rows and raise the flag
-            const Unit d = cur;
-            if (d.valid) {
-                float *orow = sout + ((int64_t)d.n * a.Dv + d.row0 + r) * kRtDk;
-                const float nan = __int_as_float(0x7fc00000);
-                for (int c = 0; c < kRtDk / 4; ++c)
-                    __stcs(reinterpret_cast<float4 *>(orow) + c, make_float4(nan, nan, nan, nan));
-            }
-            if (issuer) {
-                atomicExch(ta.wait_flag, 1u);
-                // let every copy and product this warpgroup issued land before the
-                // CTA releases its shared and tensor memory (bounded again)
-                if (last_s >= 0) mbar_wait_bounded(bar(wg, 0), (uint32_t)(last_s & 1), kRtWaitCycles);
-                for (int b2 = 0; b2 < 2; ++b2)
-                    if (last_in[b2] >= 0)
-                        mbar_wait_bounded(bar(wg, 1 + b2), (uint32_t)((last_in[b2] >> 1) & 1), kRtWaitCycles);
-                if (last_m1 >= 0) mbar_wait_bounded(bar(wg, 3), (uint32_t)(last_m1 & 1), kRtWaitCycles);
-                if (last_m2 >= 0) mbar_wait_bounded(bar(wg, 4), (uint32_t)(last_m2 & 1), kRtWaitCycles);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(wg, kRtBarDone + buf));  // the unit's buffers are free
         }
     }
     rt_fence_before();
