@@ -108,6 +108,15 @@ __device__ __forceinline__ void ldsm_x4_t_a(uint32_t (&r)[4], uint32_t a) {
                  : "r"(a));
 }
 
+// Four 8x8 bf16 matrices to shared memory: lane l gives the address of row
+// l % 8 of matrix l / 8; register i of lane (g, t) holds (row g, cols 2t, 2t+1)
+// of matrix i.
+__device__ __forceinline__ void stsm_x4_a(uint32_t a, const uint32_t (&r)[4]) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 // (x0, x1) ~ hi + lo with hi, lo packed bf16 pairs (x0 in the low half).
 // x - bf16(x) is exact in f32, so the pair carries 16 significant bits.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {

@@ -558,21 +558,28 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
             wait(bar(wg, kRtBarIn + buf), j >> 1, ok);
             const unsigned bits = pp->bits;
             {
-                // thread r writes column n = r of K^T: 16 steps, two 8-step core-matrix columns
-                uint32_t w2[8];
+                // K^T (the B operand of MMA2, K-major core matrices of 8 columns x
+                // 8 steps): warp q transposes columns 32q .. 32q+31, an 8 x 8 block
+                // at a time (ldmatrix.trans from the swizzled k rows, stmatrix into
+                // the core matrix); the halves of inactive steps are cleared
+                const int q = warp & 3, lm = lane >> 3, l8 = lane & 7, t4 = lane & 3;
+                const uint32_t mlo = (((bits >> (2 * t4)) & 1u) ? 0x0000ffffu : 0u) |
+                                     (((bits >> (2 * t4 + 1)) & 1u) ? 0xffff0000u : 0u);
+                const uint32_t mhi = (((bits >> (8 + 2 * t4)) & 1u) ? 0x0000ffffu : 0u) |
+                                     (((bits >> (9 + 2 * t4)) & 1u) ? 0xffff0000u : 0u);
 #pragma unroll
-                for (int s2 = 0; s2 < C; s2 += 2) {
-                    const uint32_t a0 = rt_kq_addr(kq, false, s2, r & ~7) + (uint32_t)(r & 7) * 2u;
-                    const uint32_t a1 = rt_kq_addr(kq, false, s2 + 1, r & ~7) + (uint32_t)(r & 7) * 2u;
-                    const uint32_t lo16 =
-                        ((bits >> s2) & 1u) ? *reinterpret_cast<const unsigned short *>(gptr(a0)) : 0u;
-                    const uint32_t hi16 =
-                        ((bits >> (s2 + 1)) & 1u) ? *reinterpret_cast<const unsigned short *>(gptr(a1)) : 0u;
-                    w2[s2 >> 1] = lo16 | (hi16 << 16);
+                for (int hh = 0; hh < 2; ++hh) {
+                    // matrices: (steps 0-7 | 8-15) x (column groups 2hh, 2hh+1 of this warp)
+                    const int sg = lm & 1, cg = 4 * q + 2 * hh + (lm >> 1);
+                    uint32_t f[4];
+                    ldsm_x4_t_a(f, rt_kq_addr(kq, false, 8 * sg + l8, 8 * cg));
+                    f[0] &= mlo;
+                    f[1] &= mhi;
+                    f[2] &= mlo;
+                    f[3] &= mhi;
+                    const uint32_t dst = gb + kRtOffB2 + (uint32_t)cg * 256u + (uint32_t)sg * 128u + (uint32_t)l8 * 16u;
+                    stsm_x4_a(dst, f);
                 }
-                unsigned char *b2 = gptr(gb + kRtOffB2 + (uint32_t)(r >> 3) * 256u + (uint32_t)(r & 7) * 16u);
-                *reinterpret_cast<uint4 *>(b2) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-                *reinterpret_cast<uint4 *>(b2 + 128) = make_uint4(w2[4], w2[5], w2[6], w2[7]);
             }
             float vv[C];
 #pragma unroll
@@ -715,12 +722,13 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                 uint32_t sv[64];
                 rt_ld16x256_x16(tm_s + ((uint32_t)(32 * q + 16 * h) << 16), sv);
                 rt_wait_ld();
+                const float2 g2 = make_float2(Gf, Gf);
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
                     __stcs(reinterpret_cast<float2 *>(o0 + 8 * m),
-                           make_float2(__uint_as_float(sv[4 * m]) * Gf, __uint_as_float(sv[4 * m + 1]) * Gf));
+                           __fmul2_rn(make_float2(__uint_as_float(sv[4 * m]), __uint_as_float(sv[4 * m + 1])), g2));
                     __stcs(reinterpret_cast<float2 *>(o1 + 8 * m),
-                           make_float2(__uint_as_float(sv[4 * m + 2]) * Gf, __uint_as_float(sv[4 * m + 3]) * Gf));
+                           __fmul2_rn(make_float2(__uint_as_float(sv[4 * m + 2]), __uint_as_float(sv[4 * m + 3])), g2));
                 }
             }
             rt_fence_before();
