@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 6
+#define GDN_ABI_VERSION 7
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st *gdn_stream_t;
@@ -355,6 +355,48 @@ const char *gdn_last_error(void);
 
 /* GDN_ABI_VERSION of the loaded library. */
 int gdn_abi_version(void);
+
+/*
+ * gdn_wait_status -- whether a bounded wait of a tensor-core kernel ran out.
+ *
+ * The tensor-core paths (the tcgen05 record kernel behind gdn_step_record and
+ * gdn_step_record_mapped, and gdn_chunk_replay) run pipelines whose stages
+ * wait on each other through mbarriers.  Every such wait gives up after a
+ * bound (about a second of GPU clock by default) instead of hanging; the
+ * kernel then writes NaN to the state rows it could not finish, lets its
+ * copies and products in flight land, and raises a device-side flag.  The
+ * call that launched it still returned GDN_OK (it only enqueues work), so a
+ * caller that wants to know reads the flag here: *expired is set to 1 if any
+ * kernel raised it since the last call, else 0, and the flag is cleared.
+ * The read is a synchronous device-to-host copy: call it after synchronising
+ * the streams that ran the calls.  The pages have no counterpart.
+ */
+gdn_status gdn_wait_status(int *expired);
+
+/*
+ * Testing hooks (the pages have no counterpart).
+ *
+ * gdn_set_wait_bound -- the bound, in GPU clock cycles, on the pipeline
+ * waits of the tensor-core kernels launched after this call (0 restores the
+ * default of 2e9 cycles).  A bound far below a kernel's normal waiting time
+ * makes its waits run out, which exercises the expiry path above without any
+ * fault: the drain after a failed wait always uses the default bound.
+ * Process-wide; not meant for production calls.
+ *
+ * gdn_inject_wait_expiry -- while on (nonzero), every tensor-core kernel
+ * launched takes, before its pipeline starts, one wait on a barrier that
+ * nothing completes, so that its bound runs out deterministically (pair it
+ * with a short gdn_set_wait_bound: with the default bound each such kernel
+ * waits about a second).  0 turns it off.
+ *
+ * gdn_force_launch_failures -- the next n calls that pass their argument
+ * checks return GDN_ERR_CUDA (with a gdn_last_error message) before touching
+ * the device, so a caller's handling of launch failures can be tested.
+ * Process-wide; 0 cancels.
+ */
+gdn_status gdn_set_wait_bound(int64_t cycles);
+gdn_status gdn_inject_wait_expiry(int on);
+gdn_status gdn_force_launch_failures(int n);
 
 #ifdef __cplusplus
 }

@@ -59,7 +59,8 @@ EXPORTED = ("gdn_step_record", "gdn_step_record_mapped", "gdn_chunk_prefill",
             "gdn_chunk_replay_workspace_size", "gdn_step_record_tstate",
             "gdn_state_replay_tstate", "gdn_state_replay",
             "gdn_state_replay_per_seq", "gqa_repeat_tiled", "gdn_status_string",
-            "gdn_last_error", "gdn_abi_version")
+            "gdn_last_error", "gdn_abi_version", "gdn_wait_status", "gdn_set_wait_bound",
+            "gdn_inject_wait_expiry", "gdn_force_launch_failures")
 
 RecordOutputs = namedtuple("RecordOutputs", "y state_out delta_log k_log g_log")
 
@@ -119,6 +120,14 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.gdn_last_error.restype = ctypes.c_char_p
     lib.gdn_abi_version.argtypes = []
     lib.gdn_abi_version.restype = ctypes.c_int
+    lib.gdn_wait_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.gdn_wait_status.restype = ctypes.c_int
+    lib.gdn_set_wait_bound.argtypes = [_I]
+    lib.gdn_set_wait_bound.restype = ctypes.c_int
+    lib.gdn_inject_wait_expiry.argtypes = [ctypes.c_int]
+    lib.gdn_inject_wait_expiry.restype = ctypes.c_int
+    lib.gdn_force_launch_failures.argtypes = [ctypes.c_int]
+    lib.gdn_force_launch_failures.restype = ctypes.c_int
 
 
 def load(path: Optional[str] = None) -> ctypes.CDLL:
@@ -424,3 +433,32 @@ def gqa_repeat_tiled(src, h: int, *, dst=None, stream=None) -> torch.Tensor:
                                  dst.numel() * dst.element_size(), _stream(dev, stream))
     _check(st, "gqa_repeat_tiled")
     return dst
+
+
+def wait_status() -> bool:
+    """Whether a bounded wait of a tensor-core kernel ran out since the last
+    call (C entry point gdn_wait_status; reads and clears the flag).  Call it
+    after synchronising the streams that ran the kernels."""
+    lib = load()
+    flag = ctypes.c_int(0)
+    _check(lib.gdn_wait_status(ctypes.byref(flag)), "gdn_wait_status")
+    return bool(flag.value)
+
+
+def set_wait_bound(cycles: int) -> None:
+    """Testing hook: the bound (GPU clock cycles) on the tensor-core kernels'
+    pipeline waits; 0 restores the default (C entry point gdn_set_wait_bound)."""
+    _check(load().gdn_set_wait_bound(int(cycles)), "gdn_set_wait_bound")
+
+
+def inject_wait_expiry(on: bool) -> None:
+    """Testing hook: while on, each tensor-core kernel takes one wait that
+    nothing completes (C entry point gdn_inject_wait_expiry)."""
+    _check(load().gdn_inject_wait_expiry(1 if on else 0), "gdn_inject_wait_expiry")
+
+
+def force_launch_failures(n: int) -> None:
+    """Testing hook: the next ``n`` calls that pass their argument checks fail
+    with GDN_ERR_CUDA before touching the device (C entry point
+    gdn_force_launch_failures)."""
+    _check(load().gdn_force_launch_failures(int(n)), "gdn_force_launch_failures")

@@ -4,6 +4,7 @@
 // dispatch_repeat_tiled_f32 ("mlx-native repeat_tiled.rs"): zero dimensions,
 // a head count that does not divide, size products that overflow and buffers
 // that are too small are invalid arguments.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -75,9 +76,30 @@ int current_sm_count(cudaError_t *err) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Testing hooks (gdn_force_launch_failures, gdn_set_wait_bound).
+constexpr long long kDefaultWaitBound = 2000000000ll;  // clock cycles, about a second
+std::atomic<int> g_forced_failures{0};
+std::atomic<long long> g_wait_bound{kDefaultWaitBound};
+std::atomic<int> g_inject_expiry{0};
+
+// Consume one forced failure, if any is pending.
+bool take_forced_failure() {
+    int n = g_forced_failures.load();
+    while (n > 0)
+        if (g_forced_failures.compare_exchange_weak(n, n - 1)) return true;
+    return false;
+}
+
+gdn_status forced_failure(const char *fn) {
+    return cuda_fail(fn, "launch (forced by gdn_force_launch_failures)", cudaErrorLaunchFailure);
+}
+
 }  // namespace
 
 namespace gdn {
+
+long long wait_bound_cycles() { return g_wait_bound.load(); }
+int inject_wait_expiry() { return g_inject_expiry.load(); }
 
 bool supported_dk(int64_t dk) {
     return dk == 32 || dk == 64 || dk == 128 || dk == 192 || dk == 256;
@@ -179,6 +201,36 @@ const char *gdn_last_error(void) { return g_last_error.c_str(); }
 
 int gdn_abi_version(void) { return GDN_ABI_VERSION; }
 
+gdn_status gdn_wait_status(int *expired) {
+    if (!expired) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_wait_status: expired must be non-NULL");
+    unsigned rec = 0, rep = 0;
+    cudaError_t e = gdn::record_tc_take_wait_flag(&rec);
+    if (e != cudaSuccess) return cuda_fail("gdn_wait_status", "record flag", e);
+    e = gdn::replay_tc_take_wait_flag(&rep);
+    if (e != cudaSuccess) return cuda_fail("gdn_wait_status", "replay flag", e);
+    *expired = (rec | rep) != 0u ? 1 : 0;
+    return ok();
+}
+
+gdn_status gdn_set_wait_bound(int64_t cycles) {
+    if (cycles < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_set_wait_bound: cycles (%lld) must be >= 0",
+                    (long long)cycles);
+    g_wait_bound.store(cycles == 0 ? kDefaultWaitBound : (long long)cycles);
+    return ok();
+}
+
+gdn_status gdn_inject_wait_expiry(int on) {
+    g_inject_expiry.store(on != 0 ? 1 : 0);
+    return ok();
+}
+
+gdn_status gdn_force_launch_failures(int n) {
+    if (n < 0) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_force_launch_failures: n (%d) must be >= 0", n);
+    g_forced_failures.store(n);
+    return ok();
+}
+
 }  // extern "C"
 
 namespace {
@@ -221,6 +273,7 @@ gdn_status record_impl(const char *fn, const void *q, const void *k, const void 
         return fail(GDN_ERR_INVALID_ARGUMENT,
                     "%s: state_out overlaps state_in without being the same buffer", fn);
 
+    if (take_forced_failure()) return forced_failure(fn);
     cudaError_t e;
     const int sms = current_sm_count(&e);
     if (e != cudaSuccess) return cuda_fail(fn, "device query", e);
@@ -283,6 +336,7 @@ gdn_status replay_impl(const char *fn, const void *delta_log, const void *k_log,
     const int64_t steps = accepted < T ? accepted : T;
     if (!accepted_per_seq && steps == 0 && state_in == state_out)
         return ok();  // identity, nothing to do
+    if (take_forced_failure()) return forced_failure(fn);
     cudaError_t e;
     const int sms = current_sm_count(&e);
     if (e != cudaSuccess) return cuda_fail(fn, "device query", e);
@@ -355,6 +409,7 @@ gdn_status chunk_prefill_impl(const char *fn, const void *q, const void *k, cons
     a.tiled_gqa = mapping == GDN_GQA_TILED;
     if ((B * Hv) > (int64_t)INT32_MAX / a.nchunks || (B * Hv) > (int64_t)INT32_MAX / a.row_blocks)
         return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large", fn);
+    if (take_forced_failure()) return forced_failure(fn);
     const cudaError_t e = gdn::launch_chunk(static_cast<gdn::DType>(dtype), (int)Dk, a,
                                             reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(fn, "launch", e);
@@ -401,6 +456,7 @@ gdn_status chunk_replay_impl(const char *fn, const void *delta_log, const void *
     if (grid > (int64_t)INT32_MAX || B * Hv > (int64_t)INT32_MAX)
         return fail(GDN_ERR_INVALID_ARGUMENT, "%s: grid too large", fn);
 
+    if (take_forced_failure()) return forced_failure(fn);
     cudaError_t e;
     const int sms = current_sm_count(&e);
     if (e != cudaSuccess) return cuda_fail(fn, "device query", e);
@@ -573,6 +629,7 @@ gdn_status gqa_repeat_tiled(const void *src, void *dst, int64_t seq, int64_t hg,
     if (overlap(src, need_src, dst, need_dst))
         return fail(GDN_ERR_INVALID_ARGUMENT, "gqa_repeat_tiled: src and dst overlap");
 
+    if (take_forced_failure()) return forced_failure("gqa_repeat_tiled");
     cudaError_t e;
     const int sms = current_sm_count(&e);
     if (e != cudaSuccess) return cuda_fail("gqa_repeat_tiled", "device query", e);

@@ -93,6 +93,9 @@ struct ReplayTcArgs {
     int64_t split_steps;   // steps per split (multiple of 32)
     int splits;            // step splits per tile (1: no partial sums)
     bool staged;           // tape rows are staged with cp.async (16-byte aligned rows)
+    unsigned *wait_flag;   // set to 1 when a bounded wait runs out
+    long long wait_cycles; // bound on the pipeline's waits
+    int inject_expiry;     // testing hook: one wait that nothing completes
 };
 
 struct RepeatArgs {
@@ -121,7 +124,12 @@ cudaError_t launch_record_f16(int dk, const RecordArgs &a, const Geometry &geo, 
 // address).
 bool record_tc_eligible(const RecordArgs &a, int dk, bool bf16);
 cudaError_t launch_record_tc(const RecordArgs &a, int sm_count, cudaStream_t s);
-cudaError_t record_tc_wait_flag(unsigned **ptr);
+// Read and clear the wait-expiry flag of each tensor-core kernel (host copy,
+// synchronous); the bound their pipeline waits use (clock cycles).
+cudaError_t record_tc_take_wait_flag(unsigned *was_set);
+cudaError_t replay_tc_take_wait_flag(unsigned *was_set);
+long long wait_bound_cycles();
+int inject_wait_expiry();
 cudaError_t launch_replay(DType dt, int dk, const ReplayArgs &a, const Geometry &geo,
                           cudaStream_t s);
 cudaError_t launch_repeat(const RepeatArgs &a, cudaStream_t s, int sm_count);

@@ -75,7 +75,8 @@ cudaError_t launch_tc(const RecordArgs &args, int sm_count, cudaStream_t st) {
     void *flag = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&flag, g_record_tc_wait_flag);
     if (e != cudaSuccess) return e;
-    RecordTcArgs ta{a, a.B * a.Hv * (a.Dv / kRtRows), static_cast<unsigned *>(flag)};
+    RecordTcArgs ta{a, a.B * a.Hv * (a.Dv / kRtRows), static_cast<unsigned *>(flag), wait_bound_cycles(),
+                    inject_wait_expiry()};
     e = cudaFuncSetAttribute(record_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRtSmem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(sm_count > 0 ? sm_count : 1, ta.nunits);
@@ -97,12 +98,16 @@ cudaError_t launch_record_tc(const RecordArgs &a, int sm_count, cudaStream_t st)
     return launch_tc(a, sm_count, st);
 }
 
-cudaError_t record_tc_wait_flag(unsigned **ptr) {
-    void *p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_record_tc_wait_flag);
+cudaError_t record_tc_take_wait_flag(unsigned *was_set) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_record_tc_wait_flag, sizeof v);
     if (e != cudaSuccess) return e;
-    *ptr = static_cast<unsigned *>(p);
-    return cudaSuccess;
+    *was_set = v;
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_record_tc_wait_flag, &zero, sizeof zero);
+    }
+    return e;
 }
 
 }  // namespace gdn

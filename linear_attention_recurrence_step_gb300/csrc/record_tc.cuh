@@ -62,7 +62,7 @@ constexpr int kRtDk = 128;         // key dimension of this kernel
 constexpr int kRtGroups = 2;       // warpgroups (units in flight) per CTA
 constexpr int kRtThreads = 192 * kRtGroups;  // per warpgroup: four row warps, a preparation warp, an issuer warp
 constexpr uint32_t kRtTmemCols = 512;   // S (128) + P (32) per warpgroup, 256 apart
-constexpr long long kRtWaitCycles = 2000000000ll;  // bound on any mbarrier wait (~1 s)
+constexpr long long kRtWaitCycles = 2000000000ll;  // default bound on an mbarrier wait (~1 s)
 
 // per-warpgroup shared memory (bytes)
 constexpr uint32_t kRtSlot = kRtRows * kRtDk * 4;           // f32 state rows; then A hi / lo
@@ -81,10 +81,11 @@ constexpr uint32_t kRtOffPrep = kRtOffB2 + kRtB2;
 constexpr uint32_t kRtGroupBytes = kRtOffPrep + 2 * kRtPrepAl;
 // mbarriers per warpgroup: 0 state landed, 1-2 inputs landed [buf], 3 MMA1
 // done, 4 MMA2 done, 5-6 preparation ready [buf], 7-8 unit finished [buf],
-// 9 operand tiles written (pass), 10 d tiles written (solve); one spare
+// 9 operand tiles written (pass), 10 d tiles written (solve), 11 never
+// completed (the testing hook gdn_inject_wait_expiry waits on it)
 constexpr int kRtBars = 12;
 constexpr int kRtBarState = 0, kRtBarIn = 1, kRtBarMma1 = 3, kRtBarMma2 = 4, kRtBarPrep = 5,
-              kRtBarDone = 7, kRtBarPass = 9, kRtBarSolve = 10;
+              kRtBarDone = 7, kRtBarPass = 9, kRtBarSolve = 10, kRtBarNever = 11;
 constexpr uint32_t kRtSmem = kRtGroups * kRtGroupBytes + kRtGroups * kRtBars * 8 + 16 + 1024;
 static_assert(kRtPrep <= kRtPrepAl, "preparation block");
 static_assert(kRtGroupBytes % 1024 == 0, "warpgroup region alignment");
@@ -180,6 +181,9 @@ struct RecordTcArgs {
     RecordArgs a;
     int64_t nunits;         // B * Hv * (Dv / 128)
     unsigned *wait_flag;    // set to 1 when a bounded wait runs out
+    long long wait_cycles;  // bound on the pipeline's waits (the drain after a
+                            // failure always waits up to kRtWaitCycles)
+    int inject_expiry;      // testing hook: one wait that nothing completes
 };
 
 __global__ void __launch_bounds__(kRtThreads, 1)
@@ -282,8 +286,8 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
             const Unit dn = unit_of(g, j + 1);
             prefetch(dn);
             // this buffer's previous unit (j - 2) is finished; the k / q rows landed
-            if (j >= 2) ok = mbar_wait_bounded(bar(g, kRtBarDone + buf), (uint32_t)(((j >> 1) - 1) & 1), kRtWaitCycles);
-            ok = ok && mbar_wait_bounded(bar(g, kRtBarIn + buf), (uint32_t)((j >> 1) & 1), kRtWaitCycles);
+            if (j >= 2) ok = mbar_wait_bounded(bar(g, kRtBarDone + buf), (uint32_t)(((j >> 1) - 1) & 1), ta.wait_cycles);
+            ok = ok && mbar_wait_bounded(bar(g, kRtBarIn + buf), (uint32_t)((j >> 1) & 1), ta.wait_cycles);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             // Gram matrices KK[u][s] = k_u . k_s and KQ[u][s] = k_u . q_s (mma.sync)
@@ -412,14 +416,14 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                 if (dn.valid) {  // the next unit's inputs, once their buffer's last unit (j - 1) is done
                     if (j >= 1)
                         ok = mbar_wait_bounded(bar(wg, kRtBarDone + (buf ^ 1)), (uint32_t)(((j - 1) >> 1) & 1),
-                                               kRtWaitCycles);
+                                               ta.wait_cycles);
                     if (!ok) break;
                     issue_in(dn, buf ^ 1);
                     last_in[buf ^ 1] = j + 1;
                 }
                 // MMA1: P = [S hi; S lo] [K; Q]^T, once the row warps wrote the operand tiles
-                ok = mbar_wait_bounded(bar(wg, kRtBarPass), (uint32_t)(j & 1), kRtWaitCycles) &&
-                     mbar_wait_bounded(bar(wg, kRtBarIn + buf), (uint32_t)((j >> 1) & 1), kRtWaitCycles);
+                ok = mbar_wait_bounded(bar(wg, kRtBarPass), (uint32_t)(j & 1), ta.wait_cycles) &&
+                     mbar_wait_bounded(bar(wg, kRtBarIn + buf), (uint32_t)((j >> 1) & 1), ta.wait_cycles);
                 if (!ok) break;
                 rt_fence_after();
 #pragma unroll
@@ -433,14 +437,14 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                 rt_commit(bar(wg, kRtBarMma1));
                 last_m1 = j;
                 // the slot is free once MMA1 has read it: the next unit's state rows
-                ok = mbar_wait_bounded(bar(wg, kRtBarMma1), (uint32_t)(j & 1), kRtWaitCycles);
+                ok = mbar_wait_bounded(bar(wg, kRtBarMma1), (uint32_t)(j & 1), ta.wait_cycles);
                 if (!ok) break;
                 if (dn.valid) {
                     issue_state(dn);
                     last_s = j + 1;
                 }
                 // MMA2: S += [D hi; D lo] K, once the row warps wrote D and K^T
-                ok = mbar_wait_bounded(bar(wg, kRtBarSolve), (uint32_t)(j & 1), kRtWaitCycles);
+                ok = mbar_wait_bounded(bar(wg, kRtBarSolve), (uint32_t)(j & 1), ta.wait_cycles);
                 if (!ok) break;
                 rt_fence_after();
                 const uint64_t db = rt_desc(gb + kRtOffB2, 128, 256, 0);
@@ -475,13 +479,20 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
         float *sout = static_cast<float *>(a.state_out);
         // a wait that runs out raises the flag at once; the warpgroup stops at
         // its next shared barrier
+        // After a failed wait the rest of the unit still arrives on every
+        // barrier (so nothing else waits in vain) but skips the tensor-memory
+        // reads that the missing product would have fed, and writes NaN as the
+        // unit's state rows.  The decision is taken per warp (tensor-memory
+        // loads are warp-wide).
         auto wait = [&](uint32_t b, int64_t phase, bool &okv) {
-            if (okv && !mbar_wait_bounded(b, (uint32_t)(phase & 1), kRtWaitCycles)) {
+            if (okv && !mbar_wait_bounded(b, (uint32_t)(phase & 1), ta.wait_cycles)) {
                 okv = false;
                 atomicExch(ta.wait_flag, 1u);
             }
+            okv = __all_sync(0xffffffffu, okv);
         };
         bool ok = true;
+        if (ta.inject_expiry) wait(bar(wg, kRtBarNever), 0, ok);  // testing hook: runs out
         for (int64_t j = 0;; ++j) {
             const Unit d = unit_of(wg, j);
             if (!d.valid) break;
@@ -590,8 +601,13 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
 
             // ---- this row's step dots, and the FP32 solve
             uint32_t pr[32];
-            rt_ld32(tm_p + lane_off, pr);
-            rt_wait_ld();
+            if (ok) {
+                rt_ld32(tm_p + lane_off, pr);
+                rt_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pr[e] = 0u;
+            }
             const unsigned direct = pp->direct;
             float dd[C];
             float phi_all = 1.f;
@@ -688,7 +704,7 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                 *reinterpret_cast<uint4 *>(a2 + 4096) = make_uint4(l8[0], l8[1], l8[2], l8[3]);
                 *reinterpret_cast<uint4 *>(a2 + 4096 + 128) = make_uint4(l8[4], l8[5], l8[6], l8[7]);
             }
-            if (phi_all != 1.f) {
+            if (phi_all != 1.f && ok) {
                 // folds in this chunk (the same in every row): S <- phi S before adding D K
 #pragma unroll 1
                 for (int c = 0; c < kRtDk / 32; ++c) {
@@ -712,7 +728,7 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
             // block, so every store instruction writes 8 rows x 32 contiguous bytes.
             wait(bar(wg, kRtBarMma2), j, ok);
             rt_fence_after();
-            const float Gf = pp->gfinal;
+            const float Gf = ok ? pp->gfinal : __int_as_float(0x7fc00000);  // NaN after a failed wait
             const int q = warp & 3;
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
@@ -720,8 +736,13 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                 float *o0 = sout + ((int64_t)d.n * a.Dv + d.row0 + rbase) * kRtDk + 2 * (lane & 3);
                 float *o1 = o0 + 8 * kRtDk;
                 uint32_t sv[64];
-                rt_ld16x256_x16(tm_s + ((uint32_t)(32 * q + 16 * h) << 16), sv);
-                rt_wait_ld();
+                if (ok) {
+                    rt_ld16x256_x16(tm_s + ((uint32_t)(32 * q + 16 * h) << 16), sv);
+                    rt_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) sv[e] = 0u;
+                }
                 const float2 g2 = make_float2(Gf, Gf);
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {

@@ -4,13 +4,37 @@
 
 namespace gdn {
 
-cudaError_t launch_replay_tc(DType dt, int dk, const ReplayTcArgs &a, cudaStream_t s, int sms) {
+namespace {
+// Set by the kernel when one of its bounded waits runs out.
+__device__ unsigned g_replay_tc_wait_flag;
+}  // namespace
+
+cudaError_t launch_replay_tc(DType dt, int dk, const ReplayTcArgs &args, cudaStream_t s, int sms) {
+    ReplayTcArgs a = args;
+    void *flag = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&flag, g_replay_tc_wait_flag);
+    if (e != cudaSuccess) return e;
+    a.wait_flag = static_cast<unsigned *>(flag);
+    a.wait_cycles = wait_bound_cycles();
+    a.inject_expiry = inject_wait_expiry();
     switch (dt) {
     case DType::F32: return launch_replay_tc_type<float>(dk, a, s, sms);
     case DType::BF16: return launch_replay_tc_type<__nv_bfloat16>(dk, a, s, sms);
     case DType::F16: return launch_replay_tc_type<__half>(dk, a, s, sms);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t replay_tc_take_wait_flag(unsigned *was_set) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_replay_tc_wait_flag, sizeof v);
+    if (e != cudaSuccess) return e;
+    *was_set = v;
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_replay_tc_wait_flag, &zero, sizeof zero);
+    }
+    return e;
 }
 
 // Steps are split over CTAs only when the tiles alone give fewer than

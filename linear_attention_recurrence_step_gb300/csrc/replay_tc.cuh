@@ -23,8 +23,9 @@
 // Rows of the tile beyond Dv and steps that are not folded enter as exact
 // zeros (never loaded), so whatever unused tape slots hold cannot reach the
 // state.  Every wait on an mbarrier is bounded (about a second of clock);
-// on expiry the CTA writes NaN to its outputs instead of hanging, releases
-// its tensor memory and exits.
+// on expiry the CTA writes NaN to its outputs instead of hanging, raises the
+// library's wait-expiry flag (gdn_wait_status), releases its tensor memory
+// and exits.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -43,7 +44,7 @@ constexpr int kTcRows = 128;       // accumulator lanes = state rows per CTA
 constexpr int kTcThreads = 256;    // eight warps: two per 32 tensor-memory lanes
 constexpr int kTcSteps = 16;       // steps staged per pipeline stage
 constexpr int kTcWeightsThreads = 256;
-constexpr long long kTcWaitCycles = 2000000000ll;  // bound on any mbarrier wait
+constexpr long long kTcWaitCycles = 2000000000ll;  // default bound on an mbarrier wait (~1 s)
 
 __host__ __device__ constexpr int tc_cols(int dk) {  // tensor-memory columns to allocate
     return dk <= 32 ? 32 : dk <= 64 ? 64 : dk <= 128 ? 128 : 256;
@@ -77,7 +78,7 @@ __device__ __forceinline__ void tc_commit(unsigned mbar) {
                  : "memory");
 }
 // Bounded wait for phase `parity` of an mbarrier; false when the bound expired.
-__device__ __forceinline__ bool mbar_wait(unsigned mbar, unsigned parity) {
+__device__ __forceinline__ bool mbar_wait(unsigned mbar, unsigned parity, long long bound = kTcWaitCycles) {
     uint32_t done = 0;
     const long long t0 = clock64();
     while (!done) {
@@ -86,7 +87,7 @@ __device__ __forceinline__ bool mbar_wait(unsigned mbar, unsigned parity) {
             : "=r"(done)
             : "r"(mbar), "r"(parity)
             : "memory");
-        if (!done && clock64() - t0 > kTcWaitCycles) return false;
+        if (!done && clock64() - t0 > bound) return false;
     }
     return true;
 }
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
     unsigned char *tail = raw0 + (STAGED ? RD * RAW : 0);
     uint64_t *mbar_mma = reinterpret_cast<uint64_t *>(tail);        // [2]
     uint32_t *taddr_s = reinterpret_cast<uint32_t *>(tail + 16);
+    uint64_t *mbar_never = reinterpret_cast<uint64_t *>(tail + 24);  // never completed (testing hook)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t tiles_rb = a.B * a.Hv * a.row_blocks;
@@ -228,6 +230,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
     if (tid == 0) {
         for (int i = 0; i < 2; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&mbar_mma[i])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(mbar_never)));
     }
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
@@ -262,7 +265,9 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
     if (STAGED) cp_async_wait_group<RD - 1>();  // stage 0 landed (this thread's pieces)
     __syncthreads();
 
-    bool ok = true;
+    // testing hook (gdn_inject_wait_expiry): one wait that nothing completes,
+    // so the pipeline's bound runs out deterministically
+    bool ok = !a.inject_expiry || mbar_wait(smem_addr(mbar_never), 0u, a.wait_cycles);
     int last_issued = nstages - 1;  // last stage whose MMAs were issued (-1: none)
     // one core matrix (8 rows x 4 steps) per warp instruction: lane -> (row % 8, step % 4)
     const int cr = lane >> 2, cs = lane & 3;
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
         const int kq = warp & 3, gq = warp >> 2;
         const int64_t tq0 = ts + 4 * kq + cs;
         const float w0 = tq0 < t_end ? wn[tq0] : 0.f;
-        if (s >= 2) ok = mbar_wait(smem_addr(&mbar_mma[s & 1]), ((s - 2) >> 1) & 1) && ok;  // buffer free
+        if (s >= 2) ok = mbar_wait(smem_addr(&mbar_mma[s & 1]), ((s - 2) >> 1) & 1, a.wait_cycles) && ok;  // buffer free
         const TIn *rD = reinterpret_cast<const TIn *>(raw0 + (s % RD) * RAW);
         const TIn *rK = reinterpret_cast<const TIn *>(raw0 + (s % RD) * RAW + align16((size_t)KB * DP * sizeof(TIn)));
         // Loads first (all independent), then the tf32 splits and the stores:
@@ -349,9 +354,12 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
         issue_raw(s + RD);  // raw slot s % RD was consumed before the barrier
     }
     if (last_issued >= 0) {
+        // the drain: always up to the default bound, so that no product is in
+        // flight when tensor memory is released
         const bool done = mbar_wait(smem_addr(&mbar_mma[last_issued & 1]), (last_issued >> 1) & 1);
         ok = ok && done;
     }
+    if (!ok && tid == 0) atomicExch(a.wait_flag, 1u);
     if (STAGED) cp_async_wait_all();  // no copy outlives the CTA
     ok = __syncthreads_and(ok);
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");

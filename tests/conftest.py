@@ -8,3 +8,26 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(autouse=True)
+def _guard_bands(request):
+    """After a GPU test, every guard band around its outputs must be intact."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import gdn_testutil
+    gdn_testutil.reset_guards()
+    yield
+    try:
+        import torch
+        if torch.cuda.is_available():
+            torch.cuda.synchronize()
+    except Exception:
+        pass
+    bad = gdn_testutil.broken_guards()
+    gdn_testutil.reset_guards()
+    assert not bad, "; ".join(bad)

@@ -115,3 +115,49 @@ def device_inputs(case, dev):
     state = to_dev(case.state, dev)
     mask = None if case.mask is None else to_dev(case.mask, dev)
     return q, k, v, g, beta, state, mask
+
+
+# ------------------------------------------------------------ guard bands
+# Canary bytes around output buffers stand in for a memory checker: an
+# output allocated with guarded_full sits between two 256-byte bands of a
+# fixed pattern, and after every GPU test (tests/conftest.py) each band
+# registered during the test must still hold it, so a kernel that writes past
+# either end of its output is caught.
+GUARD_BYTES = 256          # keeps the output 256-byte aligned
+GUARD_PATTERN = 0xA5
+_GUARDS = []
+
+
+def guarded_full(shape, fill, dtype, dev):
+    """torch.full(shape, fill) with canary bands before and after it."""
+    import torch
+    shape = tuple(int(x) for x in shape)
+    n = 1
+    for x in shape:
+        n *= x
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    raw = torch.empty(2 * GUARD_BYTES + nbytes, dtype=torch.uint8, device=dev)
+    raw.fill_(GUARD_PATTERN)
+    out = raw[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype).view(shape)
+    out.fill_(fill)
+    _GUARDS.append((raw, nbytes))
+    return out
+
+
+def guarded_like(t, fill=float("nan")):
+    return guarded_full(t.shape, fill, t.dtype, t.device)
+
+
+def reset_guards():
+    _GUARDS.clear()
+
+
+def broken_guards():
+    """Descriptions of the bands that no longer hold the pattern."""
+    bad = []
+    for i, (raw, nbytes) in enumerate(_GUARDS):
+        head = raw[:GUARD_BYTES]
+        tail = raw[GUARD_BYTES + nbytes:]
+        if not bool((head == GUARD_PATTERN).all()) or not bool((tail == GUARD_PATTERN).all()):
+            bad.append(f"guarded buffer {i} ({nbytes} bytes): a write landed outside it")
+    return bad

@@ -56,7 +56,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libgdn.so does not export {name}"
-    assert lib.gdn_abi_version() == 6
+    assert lib.gdn_abi_version() == 7
 
 
 def test_library_is_sm103a():
@@ -357,3 +357,30 @@ def test_repeat_rejects(lib, name):
 def test_python_binding_refuses_without_library(tmp_path):
     with pytest.raises(gdn.GdnError):
         gdn.load(str(tmp_path / "missing.so"))
+
+
+# ------------------------------------------------- testing hooks (no device)
+def test_forced_launch_failures_stop_before_the_device(lib):
+    """gdn_force_launch_failures(n): the next n calls that pass validation
+    return GDN_ERR_CUDA without touching the device; a call that fails
+    validation does not consume one.  Exactly n valid calls are made here (a
+    further valid call with these fake pointers would reach the device)."""
+    try:
+        assert lib.gdn_force_launch_failures(2) == OK
+        assert rec(lib, B=0) == INVALID                      # validation first, nothing consumed
+        assert rec(lib) == CUDA
+        msg = lib.gdn_last_error().decode()
+        assert msg.startswith("gdn_step_record") and "forced by gdn_force_launch_failures" in msg
+        assert rpt(lib) == CUDA
+        assert "forced" in lib.gdn_last_error().decode()
+    finally:
+        assert lib.gdn_force_launch_failures(0) == OK
+    assert lib.gdn_force_launch_failures(-1) == INVALID
+
+
+def test_wait_hooks_reject_bad_arguments(lib):
+    assert lib.gdn_set_wait_bound(-1) == INVALID
+    assert lib.gdn_set_wait_bound(0) == OK
+    assert lib.gdn_inject_wait_expiry(0) == OK
+    assert lib.gdn_wait_status(None) == INVALID
+    assert lib.gdn_last_error().decode().startswith("gdn_wait_status")

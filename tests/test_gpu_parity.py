@@ -23,8 +23,8 @@ import pytest
 
 import oracle
 import workloads
-from gdn_testutil import (assert_close, device_inputs, round_to, storage_of,
-                          tape_rounding_bound, to_dev, to_host_f64, torch_dtype)
+from gdn_testutil import (assert_close, device_inputs, guarded_full, guarded_like, round_to,
+                          storage_of, tape_rounding_bound, to_dev, to_host_f64, torch_dtype)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -45,12 +45,13 @@ def dev():
 def _alloc_outputs(case, dev, capture=True):
     dt = torch_dtype(case.dtype)
     B, T, Hv, Dv, Dk = case.B, case.T, case.Hv, case.Dv, case.Dk
-    out = dict(y=torch.full((B, T, Hv, Dv), SENTINEL, dtype=dt, device=dev),
-               delta_log=torch.full((B, T, Hv, Dv), SENTINEL, dtype=dt, device=dev),
-               state_out=torch.full((B, Hv, Dv, Dk), SENTINEL, dtype=torch.float32, device=dev))
+    # guarded: the conftest checks the canary bands around every output
+    out = dict(y=guarded_full((B, T, Hv, Dv), SENTINEL, dt, dev),
+               delta_log=guarded_full((B, T, Hv, Dv), SENTINEL, dt, dev),
+               state_out=guarded_full((B, Hv, Dv, Dk), SENTINEL, torch.float32, dev))
     if capture:
-        out["k_log"] = torch.full((B, T, Hv, Dk), SENTINEL, dtype=dt, device=dev)
-        out["g_log"] = torch.full((B, T, Hv), SENTINEL, dtype=dt, device=dev)
+        out["k_log"] = guarded_full((B, T, Hv, Dk), SENTINEL, dt, dev)
+        out["g_log"] = guarded_full((B, T, Hv), SENTINEL, dt, dev)
     return out
 
 
@@ -132,7 +133,7 @@ def test_named_workload(dev, name):
     kl = round_to(np.nan_to_num(ref["k_log"]), dt)
     gl = round_to(np.nan_to_num(ref["g_log"]), dt)
     st = gdn.gdn_state_replay(to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev), s0, mask,
-                              accepted=acc)
+                              accepted=acc, state_out=guarded_like(s0))
     ref_st = oracle.replay(workloads.widen(tape, dt), workloads.widen(kl, dt),
                            workloads.widen(gl, dt), case.f64("state"), case.mask, accepted=acc)
     assert_close(to_host_f64(st), ref_st, dt, None, "replay(host tape)")
@@ -184,7 +185,7 @@ def test_sweep(dev, spec):
     kl = round_to(np.nan_to_num(ref["k_log"]), case.dtype)
     gl = round_to(np.nan_to_num(ref["g_log"]), case.dtype)
     st = gdn.gdn_state_replay(to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev), s0, mask,
-                              accepted=case.accepted)
+                              accepted=case.accepted, state_out=guarded_like(s0))
     ref_st = oracle.replay(workloads.widen(tape, case.dtype), workloads.widen(kl, case.dtype),
                            workloads.widen(gl, case.dtype), case.f64("state"), case.mask,
                            accepted=case.accepted)
@@ -322,7 +323,8 @@ def test_repeat_bit_exact(dev, dtype):
                            (2, 2, 8, 1)]:
         src = workloads.to_storage(rng.standard_normal((seq, hg, kd)).astype(np.float32), dtype)
         want = oracle.repeat_tiled(src, h)
-        got = gdn.gqa_repeat_tiled(to_dev(src, dev), h)
+        sd = to_dev(src, dev)
+        got = gdn.gqa_repeat_tiled(sd, h, dst=guarded_full((src.shape[0], h, src.shape[2]), 0, sd.dtype, dev))
         np.testing.assert_array_equal(storage_of(got), want)
     # an offset view (not 16-byte aligned) takes the element path
     src = workloads.to_storage(rng.standard_normal((6 * 2 * 8 + 1,)).astype(np.float32), dtype)
@@ -555,7 +557,7 @@ def test_chunk_replay(dev, spec):
     s0 = to_dev(case.state, dev)
     mask = None if case.mask is None else to_dev(case.mask.astype(np.int32), dev)
     st = gdn.gdn_chunk_replay(to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev), s0, mask,
-                              accepted=case.accepted)
+                              accepted=case.accepted, state_out=guarded_like(s0))
     torch.cuda.synchronize()
     want = oracle.replay(workloads.widen(tape, dt), workloads.widen(kl, dt), workloads.widen(gl, dt),
                          case.f64("state"), case.mask, accepted=case.accepted)

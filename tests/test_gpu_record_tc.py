@@ -16,7 +16,7 @@ import pytest
 
 import oracle
 import workloads
-from gdn_testutil import assert_close, device_inputs, to_host_f64
+from gdn_testutil import assert_close, device_inputs, guarded_full, to_host_f64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -36,12 +36,13 @@ def dev():
 
 def _outputs(case, dev, capture=True):
     B, T, Hv, Dv, Dk = case.B, case.T, case.Hv, case.Dv, case.Dk
-    out = dict(y=torch.full((B, T, Hv, Dv), SENTINEL, dtype=torch.bfloat16, device=dev),
-               delta_log=torch.full((B, T, Hv, Dv), SENTINEL, dtype=torch.bfloat16, device=dev),
-               state_out=torch.full((B, Hv, Dv, Dk), SENTINEL, dtype=torch.float32, device=dev))
+    # guarded: the conftest checks the canary bands around every output
+    out = dict(y=guarded_full((B, T, Hv, Dv), SENTINEL, torch.bfloat16, dev),
+               delta_log=guarded_full((B, T, Hv, Dv), SENTINEL, torch.bfloat16, dev),
+               state_out=guarded_full((B, Hv, Dv, Dk), SENTINEL, torch.float32, dev))
     if capture:
-        out["k_log"] = torch.full((B, T, Hv, Dk), SENTINEL, dtype=torch.bfloat16, device=dev)
-        out["g_log"] = torch.full((B, T, Hv), SENTINEL, dtype=torch.bfloat16, device=dev)
+        out["k_log"] = guarded_full((B, T, Hv, Dk), SENTINEL, torch.bfloat16, dev)
+        out["g_log"] = guarded_full((B, T, Hv), SENTINEL, torch.bfloat16, dev)
     return out
 
 
