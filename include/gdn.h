@@ -25,8 +25,9 @@
  *   host thread.
  * - Floating-point tensors share one element type `dtype` (f32, bf16 or
  *   f16); the recurrent state is float32 (or `dtype` in the _tstate calls).
- *   All arithmetic is float32; values written in bf16/f16 are rounded to
- *   nearest-even.
+ *   The state and every step's scalars are float32 (see gdn_step_record for
+ *   the bf16 tensor-core paths' split operands); values written in bf16/f16
+ *   are rounded to nearest-even.
  *
  * Notation: B batch, T timesteps, Hk key heads, Hv value heads (Hv % Hk == 0,
  * G = Hv / Hk, key head of value head hv is hk = hv / G), Dk key dim, Dv
@@ -108,6 +109,25 @@ typedef enum gdn_gqa_mapping {
  *              delta_log is
  *   Dk         32, 64, 128, 192 or 256 (else GDN_ERR_UNSUPPORTED); Dv any > 0
  * Outputs must not overlap inputs (other than the in-place state).
+ *
+ * Kernels and precision.  The call picks one of three kernels; all keep the
+ * state in float32 and take every step's scalars (the decay products, the
+ * reciprocals, the innovation) in float32:
+ *   - FP32 steps (every dtype; bf16 calls of fewer than 12 steps): every
+ *     product in float32, one rounding per state entry per step.
+ *   - bf16, 12 <= T <= 16, Dk = 128, Dv a multiple of 128, v 16-byte aligned:
+ *     the tcgen05 kernel (one 16-step chunk per call, TMA-fed, accumulators
+ *     in tensor memory).
+ *   - other bf16 calls with T >= 12 and Dk of 64 or 128: mma.sync 16-step
+ *     chunks.
+ * The two tensor-core forms regroup a chunk's steps into products in which
+ * the f32 state and the f32 per-row solve values enter as two bf16 terms
+ * (hi + lo, 16 significant bits) against the exact bf16 k and q rows, with
+ * f32 accumulation: each such product carries a relative error of about
+ * 2^-17, well inside the 1e-3 that bf16 inputs are held to, but the results
+ * are not bit-identical to the FP32-step kernel (and a bf16 tape is rounded
+ * in either case).  The tcgen05 kernel solves each row's chunk in FP32.
+ * Every kernel is deterministic run to run.
  */
 gdn_status gdn_step_record(const void *q, const void *k, const void *v,
                            const void *g, const void *beta,
