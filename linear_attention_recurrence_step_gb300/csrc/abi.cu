@@ -203,12 +203,14 @@ int gdn_abi_version(void) { return GDN_ABI_VERSION; }
 
 gdn_status gdn_wait_status(int *expired) {
     if (!expired) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_wait_status: expired must be non-NULL");
-    unsigned rec = 0, rep = 0;
+    unsigned rec = 0, rep = 0, str = 0;
     cudaError_t e = gdn::record_tc_take_wait_flag(&rec);
     if (e != cudaSuccess) return cuda_fail("gdn_wait_status", "record flag", e);
     e = gdn::replay_tc_take_wait_flag(&rep);
     if (e != cudaSuccess) return cuda_fail("gdn_wait_status", "replay flag", e);
-    *expired = (rec | rep) != 0u ? 1 : 0;
+    e = gdn::replay_stream_take_wait_flag(&str);
+    if (e != cudaSuccess) return cuda_fail("gdn_wait_status", "stream replay flag", e);
+    *expired = (rec | rep | str) != 0u ? 1 : 0;
     return ok();
 }
 
@@ -347,8 +349,12 @@ gdn_status replay_impl(const char *fn, const void *delta_log, const void *k_log,
                       geo.rows_cta, geo.row_blocks, geo.tc,
                       aligned(delta_log, 16) && (Dv * eb) % 16 == 0, accepted_per_seq,
                       tstate && dtype != GDN_DTYPE_F32};
-    e = gdn::launch_replay(static_cast<gdn::DType>(dtype), (int)Dk, a, geo,
-                           reinterpret_cast<cudaStream_t>(stream));
+    bool streamed = false;
+    e = gdn::launch_replay_stream(static_cast<gdn::DType>(dtype), (int)Dk, a, sms,
+                                  reinterpret_cast<cudaStream_t>(stream), &streamed);
+    if (e == cudaSuccess && !streamed)
+        e = gdn::launch_replay(static_cast<gdn::DType>(dtype), (int)Dk, a, geo,
+                               reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(fn, "launch", e);
     return ok();
 }

@@ -132,6 +132,12 @@ long long wait_bound_cycles();
 int inject_wait_expiry();
 cudaError_t launch_replay(DType dt, int dk, const ReplayArgs &a, const Geometry &geo,
                           cudaStream_t s);
+// The persistent TMA-fed replay (replay_stream.cuh) for calls of at most 16
+// steps with Dk = 128; *launched stays false when the call is not eligible
+// (then launch_replay runs), and its wait-expiry flag.
+cudaError_t launch_replay_stream(DType dt, int dk, const ReplayArgs &a, int sm_count, cudaStream_t s,
+                                 bool *launched);
+cudaError_t replay_stream_take_wait_flag(unsigned *was_set);
 cudaError_t launch_repeat(const RepeatArgs &a, cudaStream_t s, int sm_count);
 cudaError_t launch_chunk(DType dt, int dk, const ChunkArgs &a, cudaStream_t s);
 int64_t chunk_workspace_bytes(int64_t B, int64_t T, int64_t Hv);  // -1 on overflow

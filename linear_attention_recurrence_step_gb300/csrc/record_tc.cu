@@ -1,10 +1,7 @@
 // record_tc.cu -- host side of the tcgen05 record kernel (record_tc.cuh):
 // tensor maps, eligibility and launch.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "record_tc.cuh"
+#include "tma_host.h"
 
 namespace gdn {
 
@@ -12,30 +9,6 @@ namespace {
 
 // Set by the kernel when one of its bounded waits runs out.
 __device__ unsigned g_record_tc_wait_flag;
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-bool encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *ptr, const cuuint64_t *dims,
-            const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw) {
-    PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
-    if (!fn) return false;
-    const cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, dt, (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 cudaError_t launch_tc(const RecordArgs &args, int sm_count, cudaStream_t st) {
     RecordArgs a = args;
@@ -46,7 +19,7 @@ cudaError_t launch_tc(const RecordArgs &args, int sm_count, cudaStream_t st) {
         const cuuint64_t dims[3] = {(cuuint64_t)kRtDk, (cuuint64_t)a.Dv, (cuuint64_t)(a.B * a.Hv)};
         const cuuint64_t strides[2] = {(cuuint64_t)kRtDk * 4, (cuuint64_t)a.Dv * kRtDk * 4};
         const cuuint32_t box[3] = {32, (cuuint32_t)kRtRows, 1};
-        if (!encode(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.state_in, dims, strides, box,
+        if (!tma_encode(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.state_in, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
@@ -56,9 +29,9 @@ cudaError_t launch_tc(const RecordArgs &args, int sm_count, cudaStream_t st) {
         const cuuint64_t strides[3] = {(cuuint64_t)kRtDk * 2, (cuuint64_t)(a.Hk * kRtDk * 2),
                                        (cuuint64_t)(a.T * a.Hk * kRtDk * 2)};
         const cuuint32_t box[4] = {64, 1, (cuuint32_t)kMmaChunk, 1};
-        if (!encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k, dims, strides, box,
+        if (!tma_encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.q, dims, strides, box,
+            !tma_encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.q, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
@@ -68,7 +41,7 @@ cudaError_t launch_tc(const RecordArgs &args, int sm_count, cudaStream_t st) {
         const cuuint64_t strides[3] = {(cuuint64_t)a.Dv * 2, (cuuint64_t)(a.Hv * a.Dv * 2),
                                        (cuuint64_t)(a.T * a.Hv * a.Dv * 2)};
         const cuuint32_t box[4] = {(cuuint32_t)kRtRows, 1, (cuuint32_t)kMmaChunk, 1};
-        if (!encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.v, dims, strides, box,
+        if (!tma_encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.v, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
@@ -91,7 +64,7 @@ bool record_tc_eligible(const RecordArgs &a, int dk, bool bf16) {
     // and coordinates that fit the int32 fields of a TMA box
     return bf16 && !a.tstate && dk == kRtDk && a.Dv % kRtRows == 0 && a.T >= 1 && a.T <= kMmaChunk &&
            a.vec_v && a.B * a.Hv * (a.Dv / kRtRows) <= (int64_t)INT32_MAX && a.Dv <= (int64_t)INT32_MAX &&
-           tensor_map_encoder() != nullptr;
+           tma_encoder_available();
 }
 
 cudaError_t launch_record_tc(const RecordArgs &a, int sm_count, cudaStream_t st) {

@@ -87,6 +87,30 @@ def test_chunk_replay_wait_expiry_is_reported(dev, restore_hooks):
     assert torch.equal(again, clean)
 
 
+def test_stream_replay_wait_expiry_is_reported(dev, restore_hooks):
+    """The persistent TMA-fed replay (bf16 tape, 16 steps, Dk = 128): its
+    ring waits give up, every row it could not fold is NaN, the flag is
+    raised, and the next call runs normally."""
+    case = workloads.make_config("rollback_b128_t16_bf16", batch=4)
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    rec = gdn.gdn_step_record(q, k, v, g, beta, s0, mask, capture_tape=True)
+    clean = gdn.gdn_state_replay(rec.delta_log, rec.k_log, rec.g_log, s0, mask, accepted=11)
+    torch.cuda.synchronize()
+    assert not gdn.wait_status()
+    gdn.set_wait_bound(1)
+    gdn.inject_wait_expiry(True)
+    bad = gdn.gdn_state_replay(rec.delta_log, rec.k_log, rec.g_log, s0, mask, accepted=11)
+    torch.cuda.synchronize()
+    assert gdn.wait_status()
+    assert torch.isnan(bad).all(), "both compute groups stop at their first block"
+    gdn.inject_wait_expiry(False)
+    gdn.set_wait_bound(0)
+    again = gdn.gdn_state_replay(rec.delta_log, rec.k_log, rec.g_log, s0, mask, accepted=11)
+    torch.cuda.synchronize()
+    assert not gdn.wait_status()
+    assert torch.equal(again, clean)
+
+
 def test_forced_launch_failure_enqueues_nothing(dev, restore_hooks):
     case = workloads.make_config("rollback_b128_t16_bf16", batch=2)
     q, k, v, g, beta, s0, mask = device_inputs(case, dev)
