@@ -283,6 +283,14 @@ gdn_status gdn_chunk_prefill_noalloc(const void *q, const void *k, const void *v
  * With a float32 tape written by gdn_step_record from the same snapshot and
  * mask, replay with accepted >= T reproduces record's state_out bit for bit,
  * and replay with accepted = a reproduces a record over the first a steps.
+ *
+ * Kernels: calls folding 2 to 16 steps with Dk = 128, a float32 state and
+ * 16-byte aligned delta_log rows (base aligned, Dv * element size a multiple
+ * of 16) run on a persistent kernel that streams 64-row state blocks and the
+ * tape rows by TMA (one CTA per SM); the others on the FP32 kernel (one CTA
+ * per 64-row block).  Both apply the same f32 operations in the same order,
+ * so their results are bit-identical.  The persistent kernel's waits are
+ * bounded as described at gdn_wait_status.
  */
 gdn_status gdn_state_replay(const void *delta_log, const void *k_log,
                             const void *g_log, const float *state_in,
@@ -377,11 +385,12 @@ const char *gdn_last_error(void);
 int gdn_abi_version(void);
 
 /*
- * gdn_wait_status -- whether a bounded wait of a tensor-core kernel ran out.
+ * gdn_wait_status -- whether a bounded wait of a pipelined (TMA / tcgen05) kernel ran out.
  *
- * The tensor-core paths (the tcgen05 record kernel behind gdn_step_record and
- * gdn_step_record_mapped, and gdn_chunk_replay) run pipelines whose stages
- * wait on each other through mbarriers.  Every such wait gives up after a
+ * The pipelined paths (the tcgen05 record kernel behind gdn_step_record and
+ * gdn_step_record_mapped, the persistent replay behind gdn_state_replay and
+ * gdn_state_replay_per_seq, and gdn_chunk_replay) run stages that wait on
+ * each other through mbarriers.  Every such wait gives up after a
  * bound (about a second of GPU clock by default) instead of hanging; the
  * kernel then writes NaN to the state rows it could not finish, lets its
  * copies and products in flight land, and raises a device-side flag.  The
@@ -397,13 +406,13 @@ gdn_status gdn_wait_status(int *expired);
  * Testing hooks (the pages have no counterpart).
  *
  * gdn_set_wait_bound -- the bound, in GPU clock cycles, on the pipeline
- * waits of the tensor-core kernels launched after this call (0 restores the
+ * waits of the pipelined kernels launched after this call (0 restores the
  * default of 2e9 cycles).  A bound far below a kernel's normal waiting time
  * makes its waits run out, which exercises the expiry path above without any
  * fault: the drain after a failed wait always uses the default bound.
  * Process-wide; not meant for production calls.
  *
- * gdn_inject_wait_expiry -- while on (nonzero), every tensor-core kernel
+ * gdn_inject_wait_expiry -- while on (nonzero), every pipelined kernel
  * launched takes, before its pipeline starts, one wait on a barrier that
  * nothing completes, so that its bound runs out deterministically (pair it
  * with a short gdn_set_wait_bound: with the default bound each such kernel

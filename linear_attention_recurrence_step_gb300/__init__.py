@@ -436,7 +436,7 @@ def gqa_repeat_tiled(src, h: int, *, dst=None, stream=None) -> torch.Tensor:
 
 
 def wait_status() -> bool:
-    """Whether a bounded wait of a tensor-core kernel ran out since the last
+    """Whether a bounded wait of a pipelined kernel ran out since the last
     call (C entry point gdn_wait_status; reads and clears the flag).  Call it
     after synchronising the streams that ran the kernels."""
     lib = load()
@@ -446,13 +446,13 @@ def wait_status() -> bool:
 
 
 def set_wait_bound(cycles: int) -> None:
-    """Testing hook: the bound (GPU clock cycles) on the tensor-core kernels'
+    """Testing hook: the bound (GPU clock cycles) on the pipelined kernels'
     pipeline waits; 0 restores the default (C entry point gdn_set_wait_bound)."""
     _check(load().gdn_set_wait_bound(int(cycles)), "gdn_set_wait_bound")
 
 
 def inject_wait_expiry(on: bool) -> None:
-    """Testing hook: while on, each tensor-core kernel takes one wait that
+    """Testing hook: while on, each pipelined kernel takes one wait that
     nothing completes (C entry point gdn_inject_wait_expiry)."""
     _check(load().gdn_inject_wait_expiry(1 if on else 0), "gdn_inject_wait_expiry")
 
