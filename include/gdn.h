@@ -113,11 +113,11 @@ typedef enum gdn_gqa_mapping {
  * Kernels and precision.  The call picks one of three kernels; all keep the
  * state in float32 and take every step's scalars (the decay products, the
  * reciprocals, the innovation) in float32:
- *   - FP32 steps (every dtype; bf16 calls of fewer than 12 steps): every
- *     product in float32, one rounding per state entry per step.
- *   - bf16, 12 <= T <= 16, Dk = 128, Dv a multiple of 128, v 16-byte aligned:
- *     the tcgen05 kernel (one 16-step chunk per call, TMA-fed, accumulators
- *     in tensor memory).
+ *   - FP32 steps (f32 / f16 inputs; bf16 calls the two below do not take):
+ *     every product in float32, one rounding per state entry per step.
+ *   - bf16, 7 <= T <= 16, Dk = 128, Dv a multiple of 128, v 16-byte aligned,
+ *     state in float32: the tcgen05 kernel (one 16-step chunk per call,
+ *     TMA-fed, accumulators in tensor memory).
  *   - other bf16 calls with T >= 12 and Dk of 64 or 128: mma.sync 16-step
  *     chunks.
  * The two tensor-core forms regroup a chunk's steps into products in which

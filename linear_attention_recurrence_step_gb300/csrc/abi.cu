@@ -138,7 +138,13 @@ static int pick_warps(int dk, int rw, int64_t tiles, int64_t Dv, int sm_count,
 }
 
 static constexpr int kChunk = 16;        // timesteps staged in shared memory at a time
-static constexpr int kMmaMinSteps = 12;  // shortest call routed to the tensor-core kernel
+static constexpr int kMmaMinSteps = 12;  // shortest call routed to the mma.sync chunk kernel
+// Shortest call routed to the tcgen05 record kernel (where it is eligible).
+// Its time hardly depends on the call's length (22.6-23.6 us at B = 16,
+// 58.6-59.5 us at B = 64 for 2 to 11 steps, Hv = 32, Dk = Dv = 128), while
+// the FP32 kernel's grows with every step: 22.3 against 22.7 us at 6 steps,
+// 24.5 against 22.7 at 8, 26.7 against 23.6 at 11.
+static constexpr int kTcMinSteps = 7;
 
 Geometry record_geometry(int dk, int64_t tiles, int64_t Dv, int64_t T, int esize, bool bf16,
                          int sm_count) {
@@ -288,7 +294,7 @@ gdn_status record_impl(const char *fn, const void *q, const void *k, const void 
                       aligned(v, 16) && (Dv * eb) % 16 == 0, mapping == GDN_GQA_TILED,
                       tstate && dtype != GDN_DTYPE_F32};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (geo.mma && gdn::record_tc_eligible(a, (int)Dk, dtype == GDN_DTYPE_BF16)) {
+    if ((geo.mma || T >= gdn::kTcMinSteps) && gdn::record_tc_eligible(a, (int)Dk, dtype == GDN_DTYPE_BF16)) {
         e = gdn::launch_record_tc(a, sms, s);  // one chunk on tcgen05, the TMA-fed stream
     } else {
         switch (dtype) {

@@ -1,13 +1,14 @@
 """GPU parity of the tcgen05 record path against the float64 oracle.
 
-bf16 record calls of at most 16 steps with Dk = 128 and Dv a multiple of 128
+bf16 record calls of 7 to 16 steps with Dk = 128 and Dv a multiple of 128
 run on the tensor-core kernel of record_tc.cuh (TMA-fed, accumulators in
 tensor memory).  These cases are chosen to route there and cover what that
 kernel adds: several 128-row units per tile (Dv = 256), more units than one
-wave of the persistent grid, calls shorter than the 16-step chunk, every mask
-form, the tiled GQA mapping, tape capture on and off, scale folds inside the
-chunk, in-place state, NaN in masked input slots, and the eligibility edges
-(T = 17, v not 16-byte aligned) that fall back to the other kernels.
+wave of the persistent grid, calls shorter than the 16-step chunk (down to
+the 7-step threshold and the speculative-verify shape), every mask form, the
+tiled GQA mapping, tape capture on and off, scale folds inside the chunk,
+in-place state, NaN in masked input slots, and the eligibility edges (T = 6
+and T = 17, v not 16-byte aligned) that fall back to the other kernels.
 """
 from __future__ import annotations
 
@@ -89,6 +90,8 @@ TC_SPECS = [
     dict(B=16, T=16, Hk=8, Hv=32, Dv=128, mask="bernoulli:0.8", seed=1205),  # 512 units: several per warpgroup
     dict(B=2, T=15, Hk=4, Hv=4, Dv=128, mask="all_on", seed=1206),
     dict(B=2, T=16, Hk=2, Hv=4, Dv=128, mask="all_off", seed=1207),
+    dict(B=16, T=8, Hk=16, Hv=32, Dv=128, mask="prefix", seed=1208),         # the speculative-verify shape
+    dict(B=3, T=7, Hk=2, Hv=6, Dv=256, mask="bernoulli:0.7", seed=1209),     # the shortest call routed here
 ]
 
 
@@ -153,12 +156,14 @@ def test_tc_record_ignores_masked_inputs(dev):
 
 
 def test_tc_record_eligibility_edges(dev):
-    """T = 17 (two chunks) and a v tensor that is not 16-byte aligned take the
-    other record kernels; both still match the oracle."""
-    case = workloads.make_case(B=2, T=17, Hk=2, Hv=4, Dk=128, Dv=128, dtype="bf16", seed=1240,
-                               mask="bernoulli:0.8")
-    got, _ = _record(case, dev)
-    _check(case, got)
+    """T = 6 (below the threshold), T = 17 (two chunks) and a v tensor that is
+    not 16-byte aligned take the other record kernels; all still match the
+    oracle."""
+    for T, seed in ((6, 1242), (17, 1240)):
+        case = workloads.make_case(B=2, T=T, Hk=2, Hv=4, Dk=128, Dv=128, dtype="bf16", seed=seed,
+                                   mask="bernoulli:0.8")
+        got, _ = _record(case, dev)
+        _check(case, got)
     case = workloads.make_case(B=2, T=16, Hk=2, Hv=4, Dk=128, Dv=128, dtype="bf16", seed=1241,
                                mask="bernoulli:0.8")
     q, k, v, g, beta, s0, mask = device_inputs(case, dev)
