@@ -16,7 +16,11 @@ onto its own copy of the snapshot (not the buffer record just read), and when
 one buffer set fits in L2 the steps rotate over enough sets that a set is
 read again only after twice the L2 capacity of other traffic; at the default
 size one set (1 GiB) is already far larger than L2.  Per-kernel durations
-come from event pairs around each launch inside the timed region.
+come from event pairs around each launch inside the timed region.  Beside the
+measured peak, ``roofline.same_size_copy`` gives the rate of a plain
+device-to-device copy of the workload's state size (L2-cold), the most one
+pass over that much state reaches on this GPU, and each kernel's fraction
+of it.
 
 ``--impl reference`` times the float64 CPU oracle on the same workload (a
 bounded batch sample per step) and prints the same JSON line.
@@ -399,6 +403,26 @@ def run_ours(args, rank, world, local_rank):
         step_bytes += 2 * (B * T * Hk * Dk + B * T * Hv * Dk) * eb
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
+    # ---- context for the fractions: a plain device-to-device copy of the
+    # workload's state size (read + write), L2-cold through rotating buffer
+    # pairs -- the most a single pass over that much state reaches here (the
+    # measured peak is taken at GB sizes; a short pass cannot hide its ramp).
+    state_bytes = B * Hv * Dv * Dk * 4
+    pairs = 1 if 2 * state_bytes >= 2 * L2_BYTES else -(-2 * L2_BYTES // (2 * state_bytes)) + 1
+    c_src = [torch.ones(state_bytes, dtype=torch.uint8, device=dev) for _ in range(pairs)]
+    c_dst = [torch.empty(state_bytes, dtype=torch.uint8, device=dev) for _ in range(pairs)]
+    c_reps = int(min(2000, max(20, 5e-3 * peak * 1e9 / (2 * state_bytes))))
+    for i in range(2 * pairs):
+        c_dst[i % pairs].copy_(c_src[i % pairs])
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for i in range(c_reps):
+        c_dst[i % pairs].copy_(c_src[i % pairs])
+    c1.record()
+    torch.cuda.synchronize()
+    copy_gbs = 2 * state_bytes * c_reps / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    del c_src, c_dst
+
     # ---- end to end through the C ABI with host buffers (pinned): every step
     # copies its inputs host -> device, runs both kernels and copies y, the
     # delta tape and the replayed state device -> host.  Steps are pipelined
@@ -548,13 +572,18 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes": dom_b, "bytes_counted": "active (unmasked) rows",
-                     "peak_source": peak_src},
+                     "peak_source": peak_src,
+                     "same_size_copy": {"bytes_each_way": state_bytes, "gbs": copy_gbs,
+                                        "frac_of_peak": copy_gbs / peak,
+                                        "kernel_frac_of_copy": achieved / copy_gbs}},
         "kernels": {
             "record": {"us": rec_ms * 1e3, "algorithmic_bytes": rec_b, "gbs": rec_gbs,
-                       "frac": rec_gbs / peak, "algorithmic_bytes_all_positions": rec_all,
+                       "frac": rec_gbs / peak, "frac_of_same_size_copy": rec_gbs / copy_gbs,
+                       "algorithmic_bytes_all_positions": rec_all,
                        "frac_all_positions": rec_all / (rec_ms * 1e-3) / 1e9 / peak},
             "replay": {"us": rep_ms * 1e3, "algorithmic_bytes": rep_b, "gbs": rep_gbs,
-                       "frac": rep_gbs / peak, "algorithmic_bytes_all_positions": rep_all,
+                       "frac": rep_gbs / peak, "frac_of_same_size_copy": rep_gbs / copy_gbs,
+                       "algorithmic_bytes_all_positions": rep_all,
                        "frac_all_positions": rep_all / (rep_ms * 1e-3) / 1e9 / peak},
         },
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
