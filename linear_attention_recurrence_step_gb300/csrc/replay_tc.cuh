@@ -43,7 +43,7 @@ namespace gdn {
 constexpr int kTcRows = 128;       // accumulator lanes = state rows per CTA
 constexpr int kTcThreads = 256;    // eight warps: two per 32 tensor-memory lanes
 constexpr int kTcSteps = 16;       // steps staged per pipeline stage
-constexpr int kTcWeightsThreads = 256;
+constexpr int kTcWeightsThreads = 1024;
 constexpr long long kTcWaitCycles = 2000000000ll;  // default bound on an mbarrier wait (~1 s)
 
 __host__ __device__ constexpr int tc_cols(int dk) {  // tensor-memory columns to allocate
@@ -110,12 +110,15 @@ __device__ __forceinline__ void tc_split(float x, float &hi, float &lo) {
 }
 
 // ------------------------------------------------------------ decay weights
-// One CTA per (b, hv): w_t (0 for steps that are not folded) and Gam.
+// One CTA per (b, hv): w_t (0 for steps that are not folded) and Gam.  Each
+// thread takes a segment of consecutive steps; the exclusive suffix products
+// of the segment products come from a block-wide scan (warp shuffles, then
+// one warp over the warps' totals), so no thread walks the segments in turn.
 template <typename TIn>
 __global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const ReplayTcArgs a) {
-    __shared__ float seg[kTcWeightsThreads];
-    __shared__ float suf[kTcWeightsThreads + 1];
-    const int tid = threadIdx.x;
+    constexpr int NW = kTcWeightsThreads / 32;
+    __shared__ float wtot[NW];  // each warp's product, then the product of the warps after it
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t n = blockIdx.x;
     const int64_t b = n / a.Hv, hv = n - b * a.Hv;
     int64_t steps = a.steps;
@@ -135,19 +138,33 @@ __global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const
     float p = 1.f;
 #pragma unroll 8
     for (int64_t t = s0; t < s1; ++t) p *= gfold(t);
-    seg[tid] = p;
+    // inclusive suffix product over the lanes of the warp: lanes lane..31
+    float inc = p;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float x = __shfl_down_sync(0xffffffffu, inc, o);
+        if (lane + o < 32) inc *= x;
+    }
+    float exc = __shfl_down_sync(0xffffffffu, inc, 1);  // lanes lane+1..31
+    if (lane == 31) exc = 1.f;
+    if (lane == 0) wtot[warp] = inc;
     __syncthreads();
-    if (tid == 0) {  // exclusive suffix products of the segment products
-        float r = 1.f;
-        suf[kTcWeightsThreads] = 1.f;
-        for (int i = kTcWeightsThreads - 1; i >= 0; --i) {
-            suf[i] = r;
-            r *= seg[i];
+    if (warp == 0) {  // the same over the warps' products
+        const float v = lane < NW ? wtot[lane] : 1.f;
+        float winc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float x = __shfl_down_sync(0xffffffffu, winc, o);
+            if (lane + o < 32) winc *= x;
         }
-        a.gam[n] = r;
+        float wexc = __shfl_down_sync(0xffffffffu, winc, 1);
+        if (lane == 31) wexc = 1.f;
+        __syncwarp();
+        if (lane < NW) wtot[lane] = wexc;
+        if (lane == 0) a.gam[n] = winc;
     }
     __syncthreads();
-    float run = suf[tid];
+    float run = exc * wtot[warp];
     float *w = a.w + n * a.T;
 #pragma unroll 8
     for (int64_t t = s1 - 1; t >= s0; --t) {
