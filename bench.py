@@ -18,9 +18,9 @@ read again only after twice the L2 capacity of other traffic; at the default
 size one set (1 GiB) is already far larger than L2.  Per-kernel durations
 come from event pairs around each launch inside the timed region.  Beside the
 measured peak, ``roofline.same_size_copy`` gives the rate of a plain
-device-to-device copy of the workload's state size (L2-cold), the most one
-pass over that much state reaches on this GPU, and each kernel's fraction
-of it.
+device-to-device copy moving as many bytes as the dominant kernel (L2-cold),
+the most one pass over that much data reaches on this GPU, and each
+kernel's fraction of it.
 
 ``--impl reference`` times the float64 CPU oracle on the same workload (a
 bounded batch sample per step) and prints the same JSON line.
@@ -403,25 +403,6 @@ def run_ours(args, rank, world, local_rank):
         step_bytes += 2 * (B * T * Hk * Dk + B * T * Hv * Dk) * eb
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
-    # ---- context for the fractions: a plain device-to-device copy of the
-    # workload's state size (read + write), L2-cold through rotating buffer
-    # pairs -- the most a single pass over that much state reaches here (the
-    # measured peak is taken at GB sizes; a short pass cannot hide its ramp).
-    state_bytes = B * Hv * Dv * Dk * 4
-    pairs = 1 if 2 * state_bytes >= 2 * L2_BYTES else -(-2 * L2_BYTES // (2 * state_bytes)) + 1
-    c_src = [torch.ones(state_bytes, dtype=torch.uint8, device=dev) for _ in range(pairs)]
-    c_dst = [torch.empty(state_bytes, dtype=torch.uint8, device=dev) for _ in range(pairs)]
-    c_reps = int(min(2000, max(20, 5e-3 * peak * 1e9 / (2 * state_bytes))))
-    for i in range(2 * pairs):
-        c_dst[i % pairs].copy_(c_src[i % pairs])
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    c0.record()
-    for i in range(c_reps):
-        c_dst[i % pairs].copy_(c_src[i % pairs])
-    c1.record()
-    torch.cuda.synchronize()
-    copy_gbs = 2 * state_bytes * c_reps / (c0.elapsed_time(c1) * 1e-3) / 1e9
-    del c_src, c_dst
 
     # ---- end to end through the C ABI with host buffers (pinned): every step
     # copies its inputs host -> device, runs both kernels and copies y, the
@@ -536,6 +517,26 @@ def run_ours(args, rank, world, local_rank):
     dom_b = rec_b if dominant == "record" else rep_b
     achieved = dom_b / (dom_ms * 1e-3) / 1e9
     traffic = measured_traffic(dominant, args.config)
+    # ---- context for the fractions: a plain device-to-device copy moving as
+    # many bytes as the dominant kernel (half read, half written), L2-cold
+    # through rotating buffer pairs -- what one pass over that much data
+    # reaches here (the measured peak is taken at GB sizes; a short pass
+    # cannot hide its ramp).
+    copy_each = max(1, round(dom_b / 2 / 2**20)) * 2**20  # whole MiB of float32
+    pairs = 1 if 2 * copy_each >= 2 * L2_BYTES else -(-2 * L2_BYTES // (2 * copy_each)) + 1
+    c_src = [torch.ones(copy_each // 4, dtype=torch.float32, device=dev) for _ in range(pairs)]
+    c_dst = [torch.empty(copy_each // 4, dtype=torch.float32, device=dev) for _ in range(pairs)]
+    c_reps = int(min(2000, max(20, 5e-3 * peak * 1e9 / (2 * copy_each))))
+    for i in range(2 * pairs):
+        c_dst[i % pairs].copy_(c_src[i % pairs])
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for i in range(c_reps):
+        c_dst[i % pairs].copy_(c_src[i % pairs])
+    c1.record()
+    torch.cuda.synchronize()
+    copy_gbs = 2 * copy_each * c_reps / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    del c_src, c_dst
     out = {
         "metric": METRIC,
         "value": value,
@@ -573,7 +574,7 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes": dom_b, "bytes_counted": "active (unmasked) rows",
                      "peak_source": peak_src,
-                     "same_size_copy": {"bytes_each_way": state_bytes, "gbs": copy_gbs,
+                     "same_size_copy": {"bytes_each_way": copy_each, "gbs": copy_gbs,
                                         "frac_of_peak": copy_gbs / peak,
                                         "kernel_frac_of_copy": achieved / copy_gbs}},
         "kernels": {
