@@ -7,8 +7,10 @@ kernel adds: several 128-row units per tile (Dv = 256), more units than one
 wave of the persistent grid, calls shorter than the 16-step chunk (down to
 the 7-step threshold and the speculative-verify shape), every mask form, the
 tiled GQA mapping, tape capture on and off, scale folds inside the chunk,
-in-place state, NaN in masked input slots, and the eligibility edges (T = 6
-and T = 17, v not 16-byte aligned) that fall back to the other kernels.
+in-place state, NaN in masked input slots, a state_out that is 16- but not
+32-byte aligned, and the eligibility edges
+(T = 6 and T = 17, v not 16-byte aligned) that fall back to the other
+kernels.
 """
 from __future__ import annotations
 
@@ -173,3 +175,28 @@ def test_tc_record_eligibility_edges(dev):
     assert v_off.data_ptr() % 16 != 0
     got, _ = _record(case, dev, inputs=(q, k, v_off, g, beta, s0, mask))
     _check(case, got)
+
+
+def test_tc_record_state_out_16_byte_offset(dev):
+    """A state_out that is 16- but not 32-byte aligned (the ABI asks for 16)
+    gives a result bit-identical to an aligned output, and nothing around it
+    is written."""
+    case = workloads.make_case(B=2, T=12, Hk=2, Hv=4, Dk=128, Dv=256, dtype="bf16", seed=1250,
+                               mask="bernoulli:0.8")
+    inputs = device_inputs(case, dev)
+    ref, _ = _record(case, dev, inputs=inputs)
+    assert ref["state_out"].data_ptr() % 32 == 0
+    q, k, v, g, beta, s0, mask = inputs
+    n = s0.numel()
+    raw = guarded_full((n + 8,), SENTINEL, torch.float32, dev)
+    off = (4 - (raw.data_ptr() // 4) % 8) % 8  # floats to 16 bytes past a 32-byte boundary
+    so = raw[off:off + n].view(s0.shape)
+    assert so.data_ptr() % 32 == 16
+    out = _outputs(case, dev)
+    out["state_out"] = so
+    gdn.gdn_step_record(q, k, v, g, beta, s0, mask, **out)
+    torch.cuda.synchronize()
+    assert torch.equal(so, ref["state_out"])
+    assert torch.isnan(raw[:off]).all() and torch.isnan(raw[off + n:]).all()
+    for name in ("y", "delta_log", "k_log", "g_log"):
+        assert torch.equal(out[name].view(torch.int16), ref[name].view(torch.int16)), name
