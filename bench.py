@@ -15,8 +15,12 @@ data-path collective) and the maximum time over ranks is used.  Replay folds
 onto its own copy of the snapshot (not the buffer record just read), and when
 one buffer set fits in L2 the steps rotate over enough sets that a set is
 read again only after twice the L2 capacity of other traffic; at the default
-size one set (1 GiB) is already far larger than L2.  Per-kernel durations
-come from event pairs around each launch inside the timed region.  Beside the
+size one set (1 GiB) is already far larger than L2.  The timed K steps have
+no event between their kernels (an event there delays the next kernel's
+launch by a few microseconds and keeps it from starting while the one before
+it finishes); per-kernel durations come from a second pass over the same K
+steps with an event pair around each launch (``config.kernel_timing``).
+Beside the
 measured peak, ``roofline.same_size_copy`` gives the rate of a plain
 device-to-device copy moving as many bytes as the dominant kernel (L2-cold),
 the most one pass over that much data reaches on this GPU, and each
@@ -378,10 +382,18 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(gpu_id if rank == 0 else None) as clocks:
+        # the measured pass: K steps, an event only before the first and after
+        # the last (an event between two kernels delays the second one's launch
+        # and keeps it from being scheduled while the first is finishing)
         t0.record(stream)
         for i in range(K):
-            step(evs[i])
+            step()
         t1.record(stream)
+        torch.cuda.synchronize()
+        # the same K steps again with an event before and after each kernel:
+        # each kernel's mean duration, for the roofline figures
+        for i in range(K):
+            step(evs[i])
         torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -567,6 +579,9 @@ def run_ours(args, rank, world, local_rank):
                    f"{(n_sets - 1) * set_bytes >> 20} MiB of other traffic, at least twice the "
                    f"{L2_BYTES >> 20} MiB L2)") + "; replay reads its own copy of the snapshot",
             "parallelism": f"{world} independent batch shard(s), no collective",
+            "kernel_timing": ("kernels.*.us: a second pass over the same K steps with CUDA events "
+                              "before and after each kernel; value and ms_per_step come from the "
+                              "first pass, with no event between kernels"),
         },
         "hbm_gbs_step": step_gbs,
         "hbm_frac_step": step_gbs / peak,

@@ -16,6 +16,12 @@
  *   ready when the stream has reached that point.
  * - `stream` is a cudaStream_t (the typedef below is the same type);
  *   NULL means the legacy default stream.
+ * - Kernels are enqueued as programmatic dependent launches: a kernel may
+ *   be scheduled while the kernel before it on the stream is still running,
+ *   but it reads and writes no global memory until that kernel has
+ *   completed and its writes are visible, so the stream order of every
+ *   memory access is that of ordinary launches (a kernel of the caller's
+ *   between two calls is waited for as usual).
  * - Dimensions are int64_t and must be > 0 (a zero or negative dimension is
  *   GDN_ERR_INVALID_ARGUMENT, the rule the tiled-repeat page applies to its
  *   own shapes).

@@ -159,6 +159,8 @@ __device__ __forceinline__ void widen_piece<__half>(uint4 raw, float (&out)[8]) 
 template <typename TIn, int DK>
 __global__ void __launch_bounds__(kCkLocalThreads)
 chunk_local_kernel(const ChunkArgs a) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int C = kCkC;
     constexpr int KS = DK + 4;   // f32 row stride: float4 rows u land 4 banks apart
     constexpr int CS = C + 1;
@@ -332,6 +334,8 @@ chunk_local_kernel(const ChunkArgs a) {
 template <typename TIn, int DK>
 __global__ void __launch_bounds__(kCkThreads)
 chunk_scan_kernel(const ChunkArgs a) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int C = kCkC;
     constexpr int KPW = DK / kCkWarps;   // state columns per warp
     // bf16 / f16 values are exact in tf32: the low terms of k / q operands
@@ -682,11 +686,9 @@ cudaError_t launch_chunk_dk(const ChunkArgs &a, cudaStream_t st) {
         e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
         if (e != cudaSuccess) return e;
     }
-    local<<<(unsigned)(a.B * a.Hk * a.nchunks), kCkLocalThreads, lsm, st>>>(a);
-    e = cudaGetLastError();
+    e = launch_dependent(local, (unsigned)(a.B * a.Hk * a.nchunks), kCkLocalThreads, lsm, st, a);
     if (e != cudaSuccess) return e;
-    scan<<<(unsigned)(a.B * a.Hv * a.row_blocks), kCkThreads, ssm, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(scan, (unsigned)(a.B * a.Hv * a.row_blocks), kCkThreads, ssm, st, a);
 }
 
 template <typename TIn>

@@ -16,6 +16,35 @@ namespace gdn {
 // Round a byte count up to a multiple of 16 (shared-memory carving).
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
+// ------------------------------------------------------------ dependent launch
+// A kernel launched with launch_dependent may be scheduled while the kernel
+// before it in the stream is still running (programmatic dependent launch):
+// its CTAs take SMs as the earlier kernel's CTAs leave them, do their set-up
+// (barriers, tensor memory, nothing that reads global memory) and then wait
+// in pdl_wait() until the earlier kernel has completed and its writes are
+// visible.  pdl_trigger() lets the next such kernel be scheduled; it is
+// called once every CTA of the grid is resident, so a waiting dependent CTA
+// never holds an SM that a CTA of the kernel it waits for still needs.  Each
+// thread that touches global memory executes pdl_wait() first.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                                    cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // ------------------------------------------------------------ element types
 template <typename T> struct Elem;
 

@@ -44,6 +44,8 @@ __host__ __device__ constexpr size_t record_smem_bytes(int dk, int tc, int rows,
 template <typename TIn, class Lay, bool TST>
 __global__ void __launch_bounds__(Lay::MAX_THREADS, Lay::MIN_BLOCKS)
 record_kernel(const RecordArgs a) {
+    pdl_trigger();
+    pdl_wait();
     using TS = typename std::conditional<TST, TIn, float>::type;
     constexpr int DK = Lay::DK;
     constexpr int RT = Lay::RT, NCH = Lay::NCH, L = Lay::L, RW = Lay::RW, REDV = Lay::REDV;
@@ -274,8 +276,7 @@ cudaError_t launch_record_layout(const RecordArgs &a, const Geometry &geo, cudaS
         if (e != cudaSuccess) return e;
     }
     const int64_t blocks = (int64_t)(a.B * a.Hv) * geo.row_blocks;
-    kern<<<(unsigned)blocks, geo.threads, geo.smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, (unsigned)blocks, geo.threads, geo.smem, st, a);
 }
 
 }  // namespace gdn

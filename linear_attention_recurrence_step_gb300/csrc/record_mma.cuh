@@ -151,6 +151,8 @@ __device__ __forceinline__ uint32_t lds32(const __nv_bfloat16 *p) {
 // otherwise it is float32.
 template <int DK, bool TST>
 __global__ void __launch_bounds__(32 * kMmaWarps, kMmaCtasPerSm) record_mma_kernel(const RecordArgs a) {
+    pdl_trigger();
+    pdl_wait();
     using T = __nv_bfloat16;
     using TS = typename std::conditional<TST, T, float>::type;
     constexpr int NT = DK / 8;   // 8-column blocks of a state row
@@ -591,8 +593,7 @@ cudaError_t launch_record_mma(const RecordArgs &a, const Geometry &geo, cudaStre
         if (e != cudaSuccess) return e;
     }
     const int64_t blocks = (int64_t)(a.B * a.Hv) * geo.row_blocks;
-    kern<<<(unsigned)blocks, geo.threads, geo.smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, (unsigned)blocks, geo.threads, geo.smem, st, a);
 }
 
 }  // namespace gdn

@@ -53,8 +53,7 @@ cudaError_t launch_tc(const RecordArgs &args, int sm_count, cudaStream_t st) {
     e = cudaFuncSetAttribute(record_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRtSmem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(sm_count > 0 ? sm_count : 1, ta.nunits);
-    record_tc_kernel<<<(unsigned)grid, kRtThreads, kRtSmem, st>>>(tm_s, tm_k, tm_q, tm_v, ta);
-    return cudaGetLastError();
+    return launch_dependent(record_tc_kernel, (unsigned)grid, kRtThreads, kRtSmem, st, tm_s, tm_k, tm_q, tm_v, ta);
 }
 
 }  // namespace

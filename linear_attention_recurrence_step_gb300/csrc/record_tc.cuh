@@ -250,6 +250,11 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
     __syncthreads();
     rt_fence_after();
     const uint32_t tmem0 = *tmem_slot;
+    // every CTA of the grid is resident and holds its tensor memory: the next
+    // kernel may be scheduled; this one reads nothing the previous kernel
+    // wrote before that kernel has completed
+    pdl_trigger();
+    pdl_wait();
 
     if (prep_warp) {
         // ================================================ preparation warp

@@ -6,6 +6,7 @@
 // one element) of a SOURCE row, reads it once and writes it to the h/hg
 // destination heads hh = hs, hs + hg, hs + 2 hg, ... that map to it: the copy
 // reads src once and writes dst once.
+#include "common.cuh"
 #include "launch.h"
 
 namespace gdn {
@@ -14,6 +15,8 @@ template <typename V>
 __global__ void __launch_bounds__(256) repeat_kernel(const V *__restrict__ src, V *__restrict__ dst,
                                                      int64_t seq, int64_t hg, int64_t h,
                                                      int64_t per_row) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t total = seq * hg * per_row;
     const int64_t copies = h / hg;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -36,10 +39,8 @@ static cudaError_t launch_v(const RepeatArgs &a, int64_t per_row, cudaStream_t s
     const int64_t cap = (int64_t)(sm_count > 0 ? sm_count : 152) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    repeat_kernel<V><<<(unsigned)blocks, threads, 0, s>>>(static_cast<const V *>(a.src),
-                                                          static_cast<V *>(a.dst), a.seq, a.hg,
-                                                          a.h, per_row);
-    return cudaGetLastError();
+    return launch_dependent(repeat_kernel<V>, (unsigned)blocks, threads, 0, s, static_cast<const V *>(a.src),
+                            static_cast<V *>(a.dst), a.seq, a.hg, a.h, per_row);
 }
 
 cudaError_t launch_repeat(const RepeatArgs &a, cudaStream_t s, int sm_count) {

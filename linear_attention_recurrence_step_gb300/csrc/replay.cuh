@@ -44,6 +44,8 @@ __host__ __device__ constexpr int replay_min_blocks() { return Lay::STATE <= 64 
 template <typename TIn, class Lay, bool TST>
 __global__ void __launch_bounds__(32 * kMaxWarpsPerCta, replay_min_blocks<Lay>())
 replay_kernel(const ReplayArgs a) {
+    pdl_trigger();
+    pdl_wait();
     using TS = typename std::conditional<TST, TIn, float>::type;
     constexpr int DK = Lay::DK;
     constexpr int RT = Lay::RT, NCH = Lay::NCH, L = Lay::L, RW = Lay::RW;
@@ -191,8 +193,7 @@ cudaError_t launch_replay_layout(const ReplayArgs &a, const Geometry &geo, cudaS
         if (e != cudaSuccess) return e;
     }
     const int64_t blocks = (int64_t)(a.B * a.Hv) * geo.row_blocks;
-    kern<<<(unsigned)blocks, geo.threads, geo.smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, (unsigned)blocks, geo.threads, geo.smem, st, a);
 }
 
 }  // namespace gdn

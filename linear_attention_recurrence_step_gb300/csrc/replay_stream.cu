@@ -60,8 +60,7 @@ cudaError_t launch_t(const ReplayArgs &args, int sm_count, cudaStream_t st, bool
     if (e != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(sm_count > 0 ? sm_count : 1, ra.nblocks);
     *launched = true;
-    kern<<<(unsigned)grid, kRsThreads, S::SMEM, st>>>(tm_s, tm_k, tm_d, ra);
-    return cudaGetLastError();
+    return launch_dependent(kern, (unsigned)grid, kRsThreads, S::SMEM, st, tm_s, tm_k, tm_d, ra);
 }
 
 }  // namespace

@@ -121,6 +121,8 @@ replay_stream_kernel(const __grid_constant__ CUtensorMap tm_s, const __grid_cons
         mbar_init_fence();
     }
     __syncthreads();
+    pdl_trigger();
+    pdl_wait();
 
     // blocks of this CTA: blockIdx.x + k * gridDim.x, k = 0 .. nk-1.  Block k
     // goes to compute group k % kRsGroups as that group's i-th block (i = k /

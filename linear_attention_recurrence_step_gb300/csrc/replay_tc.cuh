@@ -116,6 +116,8 @@ __device__ __forceinline__ void tc_split(float x, float &hi, float &lo) {
 // one warp over the warps' totals), so no thread walks the segments in turn.
 template <typename TIn>
 __global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const ReplayTcArgs a) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int NW = kTcWeightsThreads / 32;
     __shared__ float wtot[NW];  // each warp's product, then the product of the warps after it
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -254,6 +256,8 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
     const uint32_t tmem = *taddr_s;
+    pdl_trigger();
+    pdl_wait();
     const uint32_t idesc = tc_idesc_tf32(DK);
 
     // cp.async (16-byte pieces, every thread) of stage s's tape rows into raw
@@ -424,6 +428,8 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
 
 // S_out = Gam S_in + the partial sums of the step splits, in split order.
 __global__ void __launch_bounds__(256) replay_reduce_kernel(const ReplayTcArgs a, int dk) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t per_tile = a.Dv * dk / 4;  // float4 per tile
     const int64_t total = a.B * a.Hv * per_tile;
     const int64_t plane = a.B * a.Hv * a.Dv * dk / 4;
@@ -452,16 +458,13 @@ cudaError_t launch_replay_tc_dk(const ReplayTcArgs &a, cudaStream_t st, int sm_c
     const size_t sm = replay_tc_smem_bytes2(DK, (int)sizeof(TIn), a.staged);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    replay_weights_kernel<TIn><<<(unsigned)(a.B * a.Hv), kTcWeightsThreads, 0, st>>>(a);
-    e = cudaGetLastError();
+    e = launch_dependent(replay_weights_kernel<TIn>, (unsigned)(a.B * a.Hv), kTcWeightsThreads, 0, st, a);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(a.splits * a.B * a.Hv * a.row_blocks), kTcThreads, sm, st>>>(a);
-    e = cudaGetLastError();
+    e = launch_dependent(kern, (unsigned)(a.splits * a.B * a.Hv * a.row_blocks), kTcThreads, sm, st, a);
     if (e != cudaSuccess || a.partial == nullptr) return e;
     const int64_t total = a.B * a.Hv * a.Dv * DK / 4;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)8 * (sm_count > 0 ? sm_count : 1));
-    replay_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, DK);
-    return cudaGetLastError();
+    return launch_dependent(replay_reduce_kernel, (unsigned)blocks, 256, 0, st, a, DK);
 }
 
 template <typename TIn>
