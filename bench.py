@@ -395,6 +395,9 @@ def run_ours(args, rank, world, local_rank):
         for i in range(K):
             step(evs[i])
         torch.cuda.synchronize()
+    if gdn.wait_status():
+        raise RuntimeError("a bounded wait of a pipelined kernel ran out during the timed steps: "
+                           "the outputs and the timing are not valid")
     if dist is not None:
         dist.barrier()
     elapsed_ms = t0.elapsed_time(t1)

@@ -296,7 +296,13 @@ gdn_status gdn_chunk_prefill_noalloc(const void *q, const void *k, const void *v
  * tape rows by TMA (one CTA per SM); the others on the FP32 kernel (one CTA
  * per 64-row block).  Both apply the same f32 operations in the same order,
  * so their results are bit-identical.  The persistent kernel's waits are
- * bounded as described at gdn_wait_status.
+ * bounded as described at gdn_wait_status.  Past a fixed first share per
+ * CTA, the persistent kernel hands its blocks out from a counter in library
+ * memory, one of 256 slots taken round robin per launch and reset by the
+ * launch itself; two launches that run at the same time must not share a
+ * slot, so at most 255 other launches of this kernel may be in flight
+ * alongside one (on any streams), and one captured graph that contains it
+ * must not be instantiated twice and run concurrently.
  */
 gdn_status gdn_state_replay(const void *delta_log, const void *k_log,
                             const void *g_log, const float *state_in,

@@ -1,6 +1,7 @@
 // replay_stream.cu -- host side of the persistent TMA-fed replay
 // (replay_stream.cuh): eligibility, tensor maps and launch.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 
 #include "replay_stream.cuh"
@@ -12,6 +13,15 @@ namespace {
 
 // Set by the kernel when one of its bounded waits runs out.
 __device__ unsigned g_replay_stream_wait_flag;
+
+// Block counters of the persistent kernel, one pair per launch slot: the next
+// block to hand out and the CTAs that have finished claiming.  Launches take
+// the slots round robin; the last CTA of a launch resets its pair to zero, so
+// a slot is ready again once its launch has completed.  Two launches share a
+// slot only if kRsSchedSlots launches of this kernel are in flight at once,
+// or if two instantiations of one captured graph run at the same time.
+__device__ unsigned g_rs_sched[kRsSchedSlots][2];
+std::atomic<unsigned> g_rs_next_slot{0};
 
 template <typename TIn>
 CUtensorMapDataType tape_map_type();
@@ -53,8 +63,12 @@ cudaError_t launch_t(const ReplayArgs &args, int sm_count, cudaStream_t st, bool
     void *flag = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&flag, g_replay_stream_wait_flag);
     if (e != cudaSuccess) return e;
+    void *sched = nullptr;
+    e = cudaGetSymbolAddress(&sched, g_rs_sched);
+    if (e != cudaSuccess) return e;
+    const unsigned slot = g_rs_next_slot.fetch_add(1u, std::memory_order_relaxed) % kRsSchedSlots;
     const ReplayStreamArgs ra{a, a.B * a.Hv * a.row_blocks, box_steps, static_cast<unsigned *>(flag),
-                              wait_bound_cycles(), inject_wait_expiry()};
+                              wait_bound_cycles(), inject_wait_expiry(), static_cast<unsigned *>(sched) + 2 * slot};
     auto kern = replay_stream_kernel<TIn>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
     if (e != cudaSuccess) return e;

@@ -87,11 +87,15 @@ def test_chunk_replay_wait_expiry_is_reported(dev, restore_hooks):
     assert torch.equal(again, clean)
 
 
-def test_stream_replay_wait_expiry_is_reported(dev, restore_hooks):
+@pytest.mark.parametrize("batch", [4, 32])
+def test_stream_replay_wait_expiry_is_reported(dev, restore_hooks, batch):
     """The persistent TMA-fed replay (bf16 tape, 16 steps, Dk = 128): its
     ring waits give up, every row it could not fold is NaN, the flag is
-    raised, and the next call runs normally."""
-    case = workloads.make_config("rollback_b128_t16_bf16", batch=4)
+    raised, and the next call runs normally.  Batch 4 (256 blocks) runs on
+    each CTA's fixed share alone; batch 32 (2048 blocks) also hands blocks
+    out from the launch's counter, so a failing CTA takes every block left
+    there and writes it as NaN."""
+    case = workloads.make_config("rollback_b128_t16_bf16", batch=batch)
     q, k, v, g, beta, s0, mask = device_inputs(case, dev)
     rec = gdn.gdn_step_record(q, k, v, g, beta, s0, mask, capture_tape=True)
     clean = gdn.gdn_state_replay(rec.delta_log, rec.k_log, rec.g_log, s0, mask, accepted=11)

@@ -131,3 +131,35 @@ def test_stream_replay_f32_record_bit_exact(dev):
         st = gdn.gdn_state_replay(full.delta_log, full.k_log, full.g_log, s0, mask, accepted=a)
         torch.cuda.synchronize()
         assert torch.equal(st, sub.state_out), f"accepted={a}"
+
+
+def test_stream_replay_two_streams_and_counter_slot_reuse(dev):
+    """The persistent replay hands its blocks out from a per-launch counter
+    (one of 256 slots, reset by each launch's last CTA).  Launches alternating
+    between two streams, so that two run at once, and more launches than
+    there are slots, all give the result of a lone call.  Batch 32 has 2048
+    blocks, more than the CTAs' fixed shares, so the counter is in use."""
+    case = workloads.make_config("rollback_b128_t16_bf16", batch=32)
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    rec = gdn.gdn_step_record(q, k, v, g, beta, s0, mask, capture_tape=True)
+    ref = gdn.gdn_state_replay(rec.delta_log, rec.k_log, rec.g_log, s0, mask, accepted=11)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    per = 8  # output buffers per stream, reused in stream order
+    outs = [[torch.empty_like(s0) for _ in range(per)] for _ in streams]
+    launches = 0
+    while launches < 300:
+        for o in outs:
+            for t in o:
+                t.fill_(float("nan"))
+        torch.cuda.synchronize()
+        for i in range(per):
+            for si, st in enumerate(streams):
+                with torch.cuda.stream(st):
+                    gdn.gdn_state_replay(rec.delta_log, rec.k_log, rec.g_log, s0, mask, accepted=11,
+                                         state_out=outs[si][i])
+                launches += 1
+        torch.cuda.synchronize()
+        for si in range(len(streams)):
+            for i in range(per):
+                assert torch.equal(outs[si][i], ref), f"launch batch ending at {launches}: stream {si}, buffer {i}"
