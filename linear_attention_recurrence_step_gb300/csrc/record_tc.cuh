@@ -639,25 +639,7 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
                     }
                     dd[s] = acc;
                 }
-#pragma unroll
-                for (int s = 0; s < C; ++s) {
-                    if (!((bits >> s) & 1u)) continue;
-                    float bq = __uint_as_float(pr[C + s]);
-                    const float4 *kr = reinterpret_cast<const float4 *>(pp->KQT + s * C);
-#pragma unroll
-                    for (int q4 = 0; 4 * q4 < s; ++q4) {
-                        const float4 k4 = kr[q4];
-                        const float kv4[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (4 * q4 + e < s) bq = fmaf(dd[4 * q4 + e], kv4[e], bq);
-                    }
-                    const StepScalars S = pp->sc[s];
-                    const float delta = S.Gp * dd[s];
-                    const float yv = fmaf(S.Gp, bq, delta * S.kq);
-                    st_from_f32(yp + obase + s * ostep, yv);
-                    st_from_f32(dp + obase + s * ostep, delta);
-                }
+                // y and delta follow MMA2's issue (below): nothing of theirs feeds it
             } else {
                 // a fold of the scale inside the chunk: the serial solve of this row
                 float pa[C], pb[C];
@@ -726,6 +708,29 @@ record_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
             rt_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(wg, kRtBarSolve));
+            if (direct == 0u) {
+                // y_t = G'_t b_t + delta_t (k_t . q_t), b_t = P_q[t] + sum_{u<t} d_u (k_u . q_t),
+                // while MMA2 runs
+#pragma unroll
+                for (int s = 0; s < C; ++s) {
+                    if (!((bits >> s) & 1u)) continue;
+                    float bq = __uint_as_float(pr[C + s]);
+                    const float4 *kr = reinterpret_cast<const float4 *>(pp->KQT + s * C);
+#pragma unroll
+                    for (int q4 = 0; 4 * q4 < s; ++q4) {
+                        const float4 k4 = kr[q4];
+                        const float kv4[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * q4 + e < s) bq = fmaf(dd[4 * q4 + e], kv4[e], bq);
+                    }
+                    const StepScalars S = pp->sc[s];
+                    const float delta = S.Gp * dd[s];
+                    const float yv = fmaf(S.Gp, bq, delta * S.kq);
+                    st_from_f32(yp + obase + s * ostep, yv);
+                    st_from_f32(dp + obase + s * ostep, delta);
+                }
+            }
 
             // ---- s = G s^, streaming stores.  The accumulator is read in the
             // m16n8 fragment shape (16x256b): thread t holds rows t/4 and 8 + t/4
