@@ -666,10 +666,26 @@ def cpu_baseline(case, seconds: float):
         el = time.perf_counter() - t_start
         if el >= seconds or reps >= 1000:
             break
-    return {"value": reps * case.B * case.T / el, "unit": "tokens/s", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{reps} x full batch (B={case.B}, T={case.T}) record+replay, "
-                      f"{el:.1f} s, float64, OpenMP over (b, hv)"}
+    value = reps * case.B * case.T / el
+    sample = (f"{reps} x full batch (B={case.B}, T={case.T}) record+replay, {el:.1f} s, float64, "
+              f"OpenMP over (b, hv)")
+    # the same on one core, for about a third of the time
+    oracle.set_threads(1)
+    try:
+        t_start = time.perf_counter()
+        reps1 = 0
+        while True:
+            _oracle_step(oracle, case, inp)
+            reps1 += 1
+            el1 = time.perf_counter() - t_start
+            if el1 >= seconds / 3 or reps1 >= 1000:
+                break
+    finally:
+        oracle.set_threads(threads)
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample,
+            "host_cpus": os.cpu_count(),
+            "single_thread": {"value": reps1 * case.B * case.T / el1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{reps1} x full batch, {el1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
