@@ -9,7 +9,9 @@ be bit-identical for every tape type; each case is also held to the oracle.
 The cases cover fewer blocks than SMs and several blocks per group, ragged
 row blocks (Dv = 72, 200), every mask form, accepted = 0 / inside / T /
 beyond T, per-sequence counts (negative, 0, inside, beyond T), in-place
-state, and NaN in tape slots that are never read.
+state, NaN in tape slots that are never read, calls large enough that most
+blocks are handed out by the launch's counter rather than the CTAs' fixed
+shares, and launches on two streams at once.
 """
 from __future__ import annotations
 
@@ -67,6 +69,8 @@ SPECS = [
     dict(B=3, T=13, Hk=2, Hv=4, Dv=72, dtype="f32", mask="bernoulli:0.6", seed=1404),     # ragged blocks
     dict(B=2, T=16, Hk=1, Hv=3, Dv=200, dtype="f16", mask="all_on", seed=1405),
     dict(B=20, T=16, Hk=8, Hv=32, Dv=128, dtype="bf16", mask="bernoulli:0.8", seed=1406),  # 1280 blocks
+    # 2048 ragged blocks: past the CTAs' fixed shares, so handed out by the counter
+    dict(B=16, T=16, Hk=8, Hv=32, Dv=200, dtype="f16", mask="prefix", seed=1407),
 ]
 
 
@@ -163,3 +167,33 @@ def test_stream_replay_two_streams_and_counter_slot_reuse(dev):
         for si in range(len(streams)):
             for i in range(per):
                 assert torch.equal(outs[si][i], ref), f"launch batch ending at {launches}: stream {si}, buffer {i}"
+
+
+def test_stream_replay_counter_per_sequence_and_unused_slots(dev):
+    """Per-sequence counts and NaN in unread tape slots on a call large enough
+    (3072 blocks) that most blocks come from the launch's counter: bit-equal
+    to the FP32 replay kernel and within the oracle's tolerance."""
+    case = workloads.make_case(B=48, T=16, Hk=2, Hv=32, Dk=128, Dv=128, dtype="bf16", seed=1411,
+                               mask="bernoulli:0.8")
+    tape, kl, gl = _host_tape(case)
+    rng = np.random.default_rng(1412)
+    acc = rng.integers(-2, case.T + 5, size=case.B).astype(np.int32)
+    dacc = torch.from_numpy(acc).to(dev)
+    tape_n, kl_n, gl_n = tape.copy(), kl.copy(), gl.copy()
+    nan16 = np.uint16(0x7fc0)
+    for b, a in enumerate(np.clip(acc, 0, case.T)):
+        tape_n[b, a:] = nan16
+        kl_n[b, a:] = nan16
+        gl_n[b, a:] = nan16
+    dtape, dkl, dgl = to_dev(tape_n, dev), to_dev(kl_n, dev), to_dev(gl_n, dev)
+    _, _, _, _, _, s0, mask = device_inputs(case, dev)
+    stream = gdn.gdn_state_replay_per_seq(dtape, dkl, dgl, s0, mask, accepted=dacc,
+                                          state_out=guarded_like(s0))
+    fp32 = gdn.gdn_state_replay_per_seq(_off16(dtape), dkl, dgl, s0, mask, accepted=dacc)
+    torch.cuda.synchronize()
+    assert torch.equal(stream, fp32)
+    assert not torch.isnan(stream).any()
+    ref = oracle.replay(workloads.widen(tape, "bf16"), workloads.widen(kl, "bf16"),
+                        workloads.widen(gl, "bf16"), case.f64("state"), case.mask,
+                        accepted=acc.astype(np.int64))
+    assert_close(to_host_f64(stream), ref, "bf16", None, "per-sequence stream replay, counter-fed")
