@@ -422,30 +422,33 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the C ABI with host buffers (pinned): every step
     # copies its inputs host -> device, runs both kernels and copies y, the
     # delta tape and the replayed state device -> host.  Steps are pipelined
-    # the way a serving loop runs them: two device buffer sets, one stream
+    # the way a serving loop runs them: three device buffer sets, one stream
     # each for uploads, kernels and downloads, so the upload of step i+1 and
-    # the download of step i-1 overlap the kernels of step i.
+    # the download of step i-1 overlap the kernels of step i.  (With two sets
+    # the upload of step i+1 would wait for the download of step i-1, which
+    # shares its set, and the two copies would run one after the other.)
+    NE = 3
     e2e_steps = max(1, min(args.e2e_steps, K))
-    h_y = [torch.empty(y.shape, dtype=tdt).pin_memory() for _ in range(2)]
-    h_dl = [torch.empty(dl.shape, dtype=tdt).pin_memory() for _ in range(2)]
-    h_st = [torch.empty(s_rep.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    h_y = [torch.empty(y.shape, dtype=tdt).pin_memory() for _ in range(NE)]
+    h_dl = [torch.empty(dl.shape, dtype=tdt).pin_memory() for _ in range(NE)]
+    h_st = [torch.empty(s_rep.shape, dtype=torch.float32).pin_memory() for _ in range(NE)]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in (h_y[0], h_dl[0], h_st[0]))
-    # two device buffer sets; the uploaded state is also the snapshot replay
+    # the device buffer sets; the uploaded state is also the snapshot replay
     # folds onto (record writes s_rec, never state)
-    sets = [alloc_set(), alloc_set()]
+    sets = [alloc_set() for _ in range(NE)]
     for d in sets:
         d["snap"] = d["state"]
     s_up, s_run, s_down = (torch.cuda.Stream(dev) for _ in range(3))
     launchers = [make_launcher(d, s_run.cuda_stream) for d in sets]
-    up_done = [torch.cuda.Event() for _ in range(2)]
-    run_done = [torch.cuda.Event() for _ in range(2)]
-    down_done = [torch.cuda.Event() for _ in range(2)]
+    up_done = [torch.cuda.Event() for _ in range(NE)]
+    run_done = [torch.cuda.Event() for _ in range(NE)]
+    down_done = [torch.cuda.Event() for _ in range(NE)]
     for e in down_done:
         e.record(s_down)
 
     def e2e_step(i):
-        k = i & 1
+        k = i % NE
         d = sets[k]
         s_up.wait_event(down_done[k])   # this set's previous step is fully drained
         with torch.cuda.stream(s_up):
@@ -474,7 +477,7 @@ def run_ours(args, rank, world, local_rank):
     s_down.wait_event(e0)
     for i in range(e2e_steps):
         e2e_step(i)
-    s_down.wait_event(run_done[(e2e_steps - 1) & 1])
+    s_down.wait_event(run_done[(e2e_steps - 1) % NE])
     e1.record(s_down)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
@@ -491,7 +494,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     def e2e_step_resident(i):
-        k = i & 1
+        k = i % NE
         d = sets[k]
         s_up.wait_event(down_done[k])
         with torch.cuda.stream(s_up):
@@ -516,7 +519,7 @@ def run_ours(args, rank, world, local_rank):
     s_down.wait_event(e0)
     for i in range(e2e_steps):
         e2e_step_resident(i)
-    s_down.wait_event(run_done[(e2e_steps - 1) & 1])
+    s_down.wait_event(run_done[(e2e_steps - 1) % NE])
     e1.record(s_down)
     torch.cuda.synchronize()
     e2e_res_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
