@@ -612,7 +612,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "mode": "pinned host buffers; every input including the f32 state uploaded and "
                         "y, delta_log and the replayed state downloaded every step; uploads, kernels "
-                        "and downloads pipelined on three streams over two device buffer sets"},
+                        "and downloads pipelined on three streams over three device buffer sets"},
         "e2e_resident_state": {"value": e2e_res_value, "unit": "tokens/s",
                                "h2d_bytes_per_step": h2d_res, "d2h_bytes_per_step": d2h_res,
                                "steps": e2e_steps,
