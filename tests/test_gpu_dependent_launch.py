@@ -8,7 +8,8 @@ the next and write in place into buffers the previous call reads, through
 every launcher (tcgen05 record, persistent stream replay, FP32 record and
 replay, chunked prefill, tensor-core replay, tiled repeat).  A chain run with
 no synchronisation must give results bit-identical to the same chain with a
-device synchronisation after every call.
+device synchronisation after every call; a captured step replayed as a CUDA
+graph many times must give the eager result every time.
 """
 from __future__ import annotations
 
@@ -111,3 +112,46 @@ def test_unsynchronised_chain_is_bit_identical(dev, chain):
         same = ba == bb
         both_nan = torch.isnan(a.float()) & torch.isnan(b.float())
         assert bool((same | both_nan).all()), f"output {i} differs between the two runs"
+
+
+def test_graph_replays_reuse_the_counter_slot(dev):
+    """A captured record + replay step (the replay's blocks past its fixed
+    shares come from a per-launch counter slot, fixed in the graph) replayed
+    300 times in one stream: every replay resets the slot it used, so every
+    replay gives the eager result, and the dependent launches inside the
+    graph keep their order."""
+    case = workloads.make_config("rollback_b128_t16_bf16", batch=32)  # 2048 replay blocks: counter in use
+    q, k, v, g, beta, s0, mask = device_inputs(case, dev)
+    shp = (case.B, case.T, case.Hv, case.Dv)
+    out = dict(y=torch.empty(shp, dtype=torch.bfloat16, device=dev),
+               delta_log=torch.empty(shp, dtype=torch.bfloat16, device=dev),
+               k_log=torch.empty((case.B, case.T, case.Hv, case.Dk), dtype=torch.bfloat16, device=dev),
+               g_log=torch.empty((case.B, case.T, case.Hv), dtype=torch.bfloat16, device=dev),
+               state_out=torch.empty_like(s0))
+    s_rep = torch.empty_like(s0)
+
+    def step():
+        gdn.gdn_step_record(q, k, v, g, beta, s0, mask, **out)
+        gdn.gdn_state_replay(out["delta_log"], out["k_log"], out["g_log"], s0, mask, accepted=11,
+                             state_out=s_rep)
+
+    step()
+    torch.cuda.synchronize()
+    ref_rec, ref_rep = out["state_out"].clone(), s_rep.clone()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        step()  # warm-up on the capture stream
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step()
+    for i in range(300):
+        if i % 50 == 0:
+            out["state_out"].fill_(float("nan"))
+            s_rep.fill_(float("nan"))
+        graph.replay()
+        if i % 50 == 49:
+            torch.cuda.synchronize()
+            assert torch.equal(out["state_out"], ref_rec), f"record after replay {i}"
+            assert torch.equal(s_rep, ref_rep), f"replay after replay {i}"
