@@ -25,8 +25,8 @@
 //     S  = Gam_{C-1} S_in + (D aC) K  (rows x Dk, contraction over C)
 //
 // Accuracy: every product runs as three tf32 MMAs (a_hi b_lo + a_lo b_hi +
-// a_hi b_hi, each operand split x = hi + lo with hi = x rounded to tf32 and
-// lo = x - hi exact in f32), about 21 significant bits per product with f32
+// a_hi b_hi, each operand split x = hi + lo with hi = x truncated to tf32 and
+// lo = x - hi exact in f32), about 20 significant bits per product with f32
 // accumulation; bf16 / f16 k and q are exact in tf32, so with those inputs
 // the products with a k / q operand take two.  The state stays f32 in the
 // accumulator fragments for the whole launch.
@@ -77,13 +77,14 @@ __host__ __device__ constexpr size_t chunk_local_smem_bytes(int dk) {
 }
 
 // ------------------------------------------------------------ tf32 products
-// x ~ hi + lo: hi = x rounded to tf32 (nearest, ties away: add half a tf32
-// ulp to the bits, clear the 13 low bits), lo = x - hi exactly.  lo goes to
-// the MMA as is; the tensor core reads its tf32 part (19 high bits), which
-// leaves |error| < 2^-21 |x|.
+// x ~ hi + lo: the tensor core reads an f32 register as tf32 by dropping its
+// 13 low mantissa bits (truncation, checked on the GPU for m16n8k8 tf32), so
+// hi is x itself (read as trunc(x)) and lo = x - trunc(x), exact in f32 and
+// below 2^-10 |x|; the tensor core reads lo's tf32 part in turn, which leaves
+// |error| < 2^-20 |x|.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
-    lo = __float_as_uint(x - __uint_as_float(hi));
+    hi = __float_as_uint(x);
+    lo = __float_as_uint(x - __uint_as_float(hi & 0xffffe000u));
 }
 __device__ __forceinline__ void mma_tf32_1688(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                               uint32_t b1) {

@@ -103,10 +103,12 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
 }
-// x ~ hi + lo with hi = x rounded to tf32 and lo = x - hi (exact in f32).
+// x ~ hi + lo: the tensor core reads an f32 operand as tf32 by dropping its
+// 13 low mantissa bits (truncation, checked on the GPU for kind::tf32), so hi
+// is x itself and lo = x - trunc(x) (exact in f32, below 2^-10 |x|).
 __device__ __forceinline__ void tc_split(float x, float &hi, float &lo) {
-    hi = __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
-    lo = x - hi;
+    hi = x;
+    lo = x - __uint_as_float(__float_as_uint(x) & 0xffffe000u);
 }
 
 // ------------------------------------------------------------ decay weights
