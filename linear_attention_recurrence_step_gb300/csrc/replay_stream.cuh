@@ -129,13 +129,13 @@ replay_stream_kernel(const __grid_constant__ CUtensorMap tm_s, const __grid_cons
     pdl_trigger();
     pdl_wait();
 
-    // Blocks are handed out by this launch's counter in global memory: the
-    // producer claims them kRsBatch at a time, two batches ahead of their
-    // use, so CTAs on faster SMs take more blocks and all of them finish
-    // within about a batch of one another (after a fixed first share, below).  The CTA's k-th block goes to
-    // compute group k % kRsGroups as that group's i-th block (i = k /
-    // kRsGroups), through the group's own stages: stage (group, i % NSG), its
-    // (i / NSG)-th use.  Each barrier thus has a single consumer that waits
+    // Blocks are handed out by this launch's counter in global memory (after
+    // a fixed first share, below): the producer claims them kRsBatch at a
+    // time, two batches ahead of their use, so CTAs on faster SMs take more
+    // blocks and all of them finish within about a batch of one another.
+    // The CTA's k-th block goes to compute group k % kRsGroups as that
+    // group's i-th block (i = k / kRsGroups), through the group's own stages:
+    // stage (group, i % NSG), its (i / NSG)-th use.  Each barrier thus has a single consumer that waits
     // for its phases in order, so no waiter can see a phase of parity p still
     // pending from an earlier use and take it for the one it waits for.  The
     // block index travels in the stage's info words; kRsEnd there tells a
