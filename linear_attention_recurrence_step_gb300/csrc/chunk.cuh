@@ -72,7 +72,7 @@ __host__ __device__ constexpr size_t chunk_scan_smem_bytes(int dk, int esize) {
 }
 constexpr int kCkHeadsPerPass = 4;  // value heads of one key head processed side by side
 __host__ __device__ constexpr size_t chunk_local_smem_bytes(int dk) {
-    return (size_t)2 * kCkC * (dk + 4) * 4 + (size_t)(2 + 2 * kCkHeadsPerPass) * kCkC * (kCkC + 1) * 4 +
+    return (size_t)2 * kCkC * (dk + 4) * 4 + (size_t)(4 + 2 * kCkHeadsPerPass) * kCkC * (kCkC + 1) * 4 +
            (size_t)3 * kCkHeadsPerPass * kCkC * 4;
 }
 
@@ -166,19 +166,25 @@ chunk_local_kernel(const ChunkArgs a) {
     constexpr int KS = DK + 4;   // f32 row stride: float4 rows u land 4 banks apart
     constexpr int CS = C + 1;
     constexpr int VEC = 16 / (int)sizeof(TIn);
+    // bf16 / f16 values are exact in tf32: their Gram products take one MMA
+    constexpr bool kTf32Exact = !std::is_same<TIn, float>::value;
     extern __shared__ __align__(16) unsigned char smem[];
     float *sk = reinterpret_cast<float *>(smem);
     float *sq = sk + C * KS;
-    float *sKK = sq + C * KS;    // k_t . k_u
-    float *sKQ = sKK + C * CS;   // k_u . q_t
+    float *sGr = sq + C * KS;    // [half of Dk][KK, KQ][C][CS]
     constexpr int HP = kCkHeadsPerPass;
-    float *sA = sKQ + C * CS;    // [HP][C][CS] A[t][u], u <= t (zero above)
+    float *sA = sGr + 4 * C * CS;  // [HP][C][CS] A[t][u], u <= t (zero above)
     float *sN = sA + HP * C * CS;  // [HP][C][CS] N[t][u], u < t (zero elsewhere)
     float *sg = sN + HP * C * CS;  // [HP][C] effective g (1 on inactive steps)
     float *sb = sg + HP * C;       // [HP][C] effective beta (0 on inactive steps)
     float *sG = sb + HP * C;       // [HP][C] Gam_t
 
-    const int tid = threadIdx.x, lane = tid & 31;
+    // k_t . k_u and k_u . q_t: the two halves of the contraction, summed in a
+    // fixed order
+    auto KK = [&](int t, int u) { return sGr[t * CS + u] + sGr[(2 * C + t) * CS + u]; };
+    auto KQ = [&](int t, int u) { return sGr[(C + t) * CS + u] + sGr[(3 * C + t) * CS + u]; };
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t nch = a.nchunks;
     const int64_t m = blockIdx.x / nch;          // b * Hk + hk
     const int64_t c = blockIdx.x - m * nch;
@@ -245,20 +251,38 @@ chunk_local_kernel(const ChunkArgs a) {
     }
     __syncthreads();
 
-    // Gram entries, one (t, u) pair per thread
+    // ---- Gram blocks on the tensor cores: per product (KK, KQ) two m16n8
+    // tiles (steps t 0-15 x u 0-7, 8-15), each contracted over the two halves
+    // of Dk: eight tile-halves, one per warp.  A = k or q rows (m = step t),
+    // B = k rows (n = step u), both read straight from the f32 rows; f32 rows
+    // take three tf32 products (hi / lo split), about 20 significant bits.
+    static_assert(kCkLocalThreads == 256 && kCkC == 16, "one tile-half per warp");
     {
-        const int t = tid >> 4, u = tid & 15;
-        float kk = 0.f, kq = 0.f;
-#pragma unroll 4
-        for (int x = 0; x < DK; x += 4) {
-            const float4 ku = *reinterpret_cast<const float4 *>(sk + u * KS + x);
-            const float4 kt = *reinterpret_cast<const float4 *>(sk + t * KS + x);
-            const float4 qt = *reinterpret_cast<const float4 *>(sq + t * KS + x);
-            kk = fmaf(kt.x, ku.x, fmaf(kt.y, ku.y, fmaf(kt.z, ku.z, fmaf(kt.w, ku.w, kk))));
-            kq = fmaf(qt.x, ku.x, fmaf(qt.y, ku.y, fmaf(qt.z, ku.z, fmaf(qt.w, ku.w, kq))));
+        constexpr int KH = DK / 2;
+        const int g8 = lane >> 2, t4 = lane & 3;
+        const int h = warp >> 2, which = (warp >> 1) & 1, nt = warp & 1;
+        const float *Ar = (which ? sq : sk) + g8 * KS + h * KH + t4;
+        const float *Br = sk + (8 * nt + g8) * KS + h * KH + t4;
+        float dm[4] = {0.f, 0.f, 0.f, 0.f}, ds[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KH / 8; ++ks) {
+            const float av[4] = {Ar[8 * ks], Ar[8 * KS + 8 * ks], Ar[8 * ks + 4], Ar[8 * KS + 8 * ks + 4]};
+            uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_tf32(av[e], ah[e], al[e]);
+            split_tf32(Br[8 * ks], bh0, bl0);
+            split_tf32(Br[8 * ks + 4], bh1, bl1);
+            if constexpr (!kTf32Exact) {
+                mma_tf32_1688(ds, al, bh0, bh1);
+                mma_tf32_1688(ds, ah, bl0, bl1);
+            }
+            mma_tf32_1688(dm, ah, bh0, bh1);
         }
-        sKK[t * CS + u] = kk;
-        sKQ[t * CS + u] = kq;
+        float *dst = sGr + ((2 * h + which) * C + g8) * CS + 8 * nt + 2 * t4;
+        dst[0] = dm[0] + ds[0];
+        dst[1] = dm[1] + ds[1];
+        dst[8 * CS] = dm[2] + ds[2];
+        dst[8 * CS + 1] = dm[3] + ds[3];
     }
 
     // the value heads that read key head hk, up to kCkHeadsPerPass at a time:
@@ -286,7 +310,7 @@ chunk_local_kernel(const ChunkArgs a) {
             float p = 1.f;
             for (int x = u + 1; x <= t; ++x) p *= gh[x];
             sA[(i * C + t) * CS + u] = u <= t ? p : 0.f;
-            sN[(i * C + t) * CS + u] = u < t ? sb[i * C + t] * p * sKK[t * CS + u] : 0.f;
+            sN[(i * C + t) * CS + u] = u < t ? sb[i * C + t] * p * KK(t, u) : 0.f;
             if (u == 0) {
                 float Gm = 1.f;
                 for (int x = 0; x <= t; ++x) Gm *= gh[x];
@@ -319,7 +343,7 @@ chunk_local_kernel(const ChunkArgs a) {
             for (int e = ft; e < nh * C * C; e += nf) {
                 const int i = e / (C * C), j = e - i * C * C, t = j >> 4, u = j & 15;
                 float *ws = a.workspace + ((b * a.Hv + hv_of(i)) * nch + c) * kCkWsFloats;
-                ws[C * C + j] = u <= t ? sA[(i * C + t) * CS + u] * sKQ[t * CS + u] : 0.f;  // Mq
+                ws[C * C + j] = u <= t ? sA[(i * C + t) * CS + u] * KQ(t, u) : 0.f;  // Mq
             }
             for (int e = ft; e < nh * 2 * C; e += nf) {
                 const int i = e / (2 * C), j = e - i * 2 * C;
