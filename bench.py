@@ -88,9 +88,9 @@ def algorithmic_bytes(case, accepted: int, capture: bool = True):
 
 
 def algorithmic_bytes_all_positions(case, accepted: int, capture: bool = True):
-    """The same, counting every position whether its mask is on or off (the
-    survey's accounting): record moves every (b, t) row, replay every (b, t)
-    row with t < accepted."""
+    """The same, counting every position whether its mask is on or off:
+    record moves every (b, t) row, replay every (b, t) row with t < accepted
+    (an upper bound on the bytes a masked call has to move)."""
     eb = workloads.elem_size(case.dtype)
     B, T, Hk, Hv, Dk, Dv = case.B, case.T, case.Hk, case.Hv, case.Dk, case.Dv
     state = B * Hv * Dv * Dk * 4
