@@ -294,6 +294,17 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
     int last_issued = nstages - 1;  // last stage whose MMAs were issued (-1: none)
     // one core matrix (8 rows x 4 steps) per warp instruction: lane -> (row % 8, step % 4)
     const int cr = lane >> 2, cs = lane & 3;
+    // warp w fills core matrices cm = w + 8 j: step quad w % 4, row / column
+    // group 2 j + w / 4 -- one step per lane per stage
+    const int kq = warp & 3, gq = warp >> 2;
+    // the decay weight of this lane's step, loaded four stages ahead (a
+    // global load the fill depends on: issued in its own stage it would stall
+    // every stage for a DRAM round trip)
+    auto weight_of = [&](int s) {
+        const int64_t t = t_begin + (int64_t)s * KB + 4 * kq + cs;
+        return s < nstages && t < t_end ? wn[t] : 0.f;
+    };
+    float wq0 = weight_of(0), wq1 = weight_of(1), wq2 = weight_of(2), wq3 = weight_of(3);
     for (int s = 0; s < nstages; ++s) {
         unsigned char *buf = smem + (s & 1) * CANON;
         float *Ah = reinterpret_cast<float *>(buf);
@@ -301,11 +312,12 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
         float *Bh = reinterpret_cast<float *>(buf + 2 * A_BYTES);
         float *Bl = reinterpret_cast<float *>(buf + 2 * A_BYTES + B_BYTES);
         const int64_t ts = t_begin + (int64_t)s * KB;
-        // warp w fills core matrices cm = w + 8 j: step quad w % 4, row / column
-        // group 2 j + w / 4 -- one step per lane per stage
-        const int kq = warp & 3, gq = warp >> 2;
         const int64_t tq0 = ts + 4 * kq + cs;
-        const float w0 = tq0 < t_end ? wn[tq0] : 0.f;
+        const float w0 = wq0;
+        wq0 = wq1;
+        wq1 = wq2;
+        wq2 = wq3;
+        wq3 = weight_of(s + 4);
         if (s >= 2) ok = mbar_wait(smem_addr(&mbar_mma[s & 1]), ((s - 2) >> 1) & 1, a.wait_cycles) && ok;  // buffer free
         const TIn *rD = reinterpret_cast<const TIn *>(raw0 + (s % RD) * RAW);
         const TIn *rK = reinterpret_cast<const TIn *>(raw0 + (s % RD) * RAW + align16((size_t)KB * DP * sizeof(TIn)));
