@@ -139,9 +139,30 @@ __global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const
         const bool on = t < steps && (!a.mask || a.mask[b * a.T + t] != 0u);
         return on ? gv : 1.f;
     };
+    // Up to kWCache steps per thread (T <= kWCache * threads) stay in
+    // registers between the two passes, loaded all at once; longer tapes walk
+    // the steps and load them again in the second pass.  The products are
+    // taken in the same order either way.
+    constexpr int kWCache = 8;
+    const bool cached = L <= kWCache;
+    float gc[kWCache];
+    unsigned onm = 0u;
     float p = 1.f;
-#pragma unroll 8
-    for (int64_t t = s0; t < s1; ++t) p *= gfold(t);
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kWCache; ++i) {
+            const int64_t t = s0 + i;
+            const bool in = t < s1;
+            const float gv = in ? ld_f32(glp + (b * a.T + t) * a.Hv + hv) : 1.f;
+            const bool on = in && t < steps && (!a.mask || a.mask[b * a.T + t] != 0u);
+            gc[i] = on ? gv : 1.f;
+            onm |= on ? 1u << i : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < kWCache; ++i) p *= gc[i];
+    } else {
+        for (int64_t t = s0; t < s1; ++t) p *= gfold(t);
+    }
     // inclusive suffix product over the lanes of the warp: lanes lane..31
     float inc = p;
 #pragma unroll
@@ -170,12 +191,23 @@ __global__ void __launch_bounds__(kTcWeightsThreads) replay_weights_kernel(const
     __syncthreads();
     float run = exc * wtot[warp];
     float *w = a.w + n * a.T;
-#pragma unroll 8
-    for (int64_t t = s1 - 1; t >= s0; --t) {
-        const bool on = t < steps && (!a.mask || a.mask[b * a.T + t] != 0u);
-        const float gv = ld_f32(glp + (b * a.T + t) * a.Hv + hv);
-        w[t] = on ? run : 0.f;
-        run = on ? run * gv : run;
+    if (cached) {
+#pragma unroll
+        for (int i = kWCache - 1; i >= 0; --i) {
+            const int64_t t = s0 + i;
+            if (t < s1) {
+                const bool on = (onm >> i) & 1u;
+                w[t] = on ? run : 0.f;
+                run = on ? run * gc[i] : run;
+            }
+        }
+    } else {
+        for (int64_t t = s1 - 1; t >= s0; --t) {
+            const bool on = t < steps && (!a.mask || a.mask[b * a.T + t] != 0u);
+            const float gv = ld_f32(glp + (b * a.T + t) * a.Hv + hv);
+            w[t] = on ? run : 0.f;
+            run = on ? run * gv : run;
+        }
     }
 }
 
@@ -454,8 +486,23 @@ __global__ void __launch_bounds__(256) replay_reduce_kernel(const ReplayTcArgs a
          i += (int64_t)gridDim.x * blockDim.x) {
         const float gam = a.gam[i / per_tile];
         const float4 x = __ldcs(si + i);
+        // the first eight partials are loaded before any is added (one
+        // round trip instead of one per split); the sum keeps split order
+        constexpr int kBatch = 8;
+        float4 pb[kBatch];
+#pragma unroll
+        for (int s = 0; s < kBatch; ++s)
+            if (s < a.splits) pb[s] = __ldcs(pp + s * plane + i);
         float4 r = make_float4(gam * x.x, gam * x.y, gam * x.z, gam * x.w);
-        for (int s = 0; s < a.splits; ++s) {
+#pragma unroll
+        for (int s = 0; s < kBatch; ++s)
+            if (s < a.splits) {
+                r.x += pb[s].x;
+                r.y += pb[s].y;
+                r.z += pb[s].z;
+                r.w += pb[s].w;
+            }
+        for (int s = kBatch; s < a.splits; ++s) {
             const float4 p = __ldcs(pp + s * plane + i);
             r.x += p.x;
             r.y += p.y;
