@@ -596,6 +596,27 @@ def test_chunk_replay_long_per_sequence_and_unused_slots(dev):
     assert torch.equal(s1, st)
 
 
+@pytest.mark.parametrize("T,accepted", [(8192, 8192), (9000, 8777)])
+def test_chunk_replay_tape_beyond_register_cache(dev, T, accepted):
+    """One head with a long tape: the decay-weights kernel keeps up to 8192
+    steps per tile in registers (eight per thread), so T = 8192 is its last
+    cached length and T = 9000 walks the steps and loads them again for the
+    suffix pass; the steps split over well over eight CTAs, so the reduce
+    adds partials past its first batch of eight."""
+    case = workloads.make_case(B=1, T=T, Hk=1, Hv=1, Dk=64, Dv=32, dtype="f32", seed=911 + T,
+                               g_range=(0.999, 1.0), mask="bernoulli:0.9", accepted=accepted)
+    ref = oracle.record(*_oracle_inputs(case))
+    tape, kl, gl = _host_tape(case, ref)
+    s0 = to_dev(case.state, dev)
+    mask = to_dev(case.mask.astype(np.int32), dev)
+    st = gdn.gdn_chunk_replay(to_dev(tape, dev), to_dev(kl, dev), to_dev(gl, dev), s0, mask,
+                              accepted=accepted, state_out=guarded_like(s0))
+    torch.cuda.synchronize()
+    want = oracle.replay(tape.astype(np.float64), kl.astype(np.float64), gl.astype(np.float64),
+                         case.f64("state"), case.mask, accepted=accepted)
+    assert_close(to_host_f64(st), want, "f32", None, "long single-head replay")
+
+
 # ------------------------------------------------ state stored in T
 @pytest.mark.parametrize("dtype,Dk,T", [("bf16", 128, 16), ("bf16", 64, 37), ("bf16", 128, 5),
                                          ("f16", 128, 16), ("f16", 64, 9)])
