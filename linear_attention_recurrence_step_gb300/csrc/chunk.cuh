@@ -402,14 +402,26 @@ chunk_scan_kernel(const ChunkArgs a) {
     const TIn *vp = static_cast<const TIn *>(a.v);
     const bool vec_v = a.vec_v && vlim == kCkRows;
 
+    // ---- mask bits of a chunk: lane tt's mask word, loaded a chunk before
+    // its bits are formed, so no step of the loop waits on a mask load
+    auto mask_word = [&](int64_t cc) {
+        const int64_t t = cc * C + lane;
+        return a.mask && cc < nch && lane < C && t < a.T ? __ldg(a.mask + b * a.T + t) : 1u;
+    };
+    auto bits_of = [&](int64_t cc, uint32_t word) {  // the same answer on every lane
+        if (cc >= nch) return 0u;
+        const int tcnt = (int)min((int64_t)C, a.T - cc * C);
+        if (!a.mask) return tcnt >= 32 ? 0xffffffffu : ((1u << tcnt) - 1u);
+        return __ballot_sync(0xffffffffu, lane < tcnt && word != 0u);
+    };
+
     // ---- issue chunk cc into ring slot sl (an empty group past the end).
     // Rows of inactive steps are zeroed, never copied: every product of the
     // chunk multiplies them (by zero coefficients, which must not meet NaN).
-    auto issue = [&](int64_t cc, int sl) {
+    auto issue = [&](int64_t cc, int sl, unsigned bits) {
         if (cc < nch) {
             const int64_t t0 = cc * C;
             const int tcnt = (int)min((int64_t)C, a.T - t0);
-            const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
             const TIn *ksrc = kp + ((b * a.T + t0) * a.Hk + hk) * DK;
             const TIn *qsrc = qp + ((b * a.T + t0) * a.Hk + hk) * DK;
             const int64_t kq_stride = a.Hk * DK;
@@ -473,8 +485,11 @@ chunk_scan_kernel(const ChunkArgs a) {
         }
     }
 
-    issue(0, 0);
-    issue(1, 1);
+    // bits of chunks c and c + 1, and the mask word of chunk c + 2
+    unsigned bits_c = bits_of(0, mask_word(0)), bits_c1 = bits_of(1, mask_word(1));
+    uint32_t word_c2 = mask_word(2);
+    issue(0, 0, bits_c);
+    issue(1, 1, bits_c1);
     cp_async_wait_group<1>();
     __syncthreads();
 
@@ -532,7 +547,9 @@ chunk_scan_kernel(const ChunkArgs a) {
         }
         cp_async_wait_group<0>();
         __syncthreads();  // partials of chunk c and the inputs of chunk c+1 are visible
-        issue(c + 2, sl2);
+        const unsigned bits_c2 = bits_of(c + 2, word_c2);
+        word_c2 = mask_word(c + 3);  // used one chunk from now
+        issue(c + 2, sl2, bits_c2);
 
         // ---- sum the four partials and scale by Gam (P_k for every warp; the
         // y warps also P_q of their n-tile)
@@ -609,7 +626,7 @@ chunk_scan_kernel(const ChunkArgs a) {
                 for (int e = 0; e < 4; ++e) D[nt][e] += Da[nt][e] + Db[nt][e];
         }
 
-        const unsigned bits = chunk_bits(a.mask ? a.mask + b * a.T + t0 : nullptr, tcnt, lane);
+        const unsigned bits = bits_c;
         if (out_warp) {
             float o[4];
             if (ywarp) {
@@ -681,6 +698,8 @@ chunk_scan_kernel(const ChunkArgs a) {
         }
         sl = sl == 2 ? 0 : sl + 1;
         sl2 = sl2 == 2 ? 0 : sl2 + 1;
+        bits_c = bits_c1;
+        bits_c1 = bits_c2;
     }
     cp_async_wait_group<0>();
 
