@@ -90,7 +90,7 @@ struct ReplayTcArgs {
     int64_t B, T, Hv, Dv;
     int64_t steps;         // min(accepted, T) (acc_b null) or T
     int64_t row_blocks;    // ceil(Dv / 128)
-    int64_t split_steps;   // steps per split (multiple of 32)
+    int64_t split_steps;   // steps per split (a multiple of the 16-step stage)
     int splits;            // step splits per tile (1: no partial sums)
     bool staged;           // tape rows are staged with cp.async (16-byte aligned rows)
     unsigned *wait_flag;   // set to 1 when a bounded wait runs out

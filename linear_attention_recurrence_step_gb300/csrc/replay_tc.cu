@@ -38,8 +38,11 @@ cudaError_t replay_tc_take_wait_flag(unsigned *was_set) {
 }
 
 // Steps are split over CTAs only when the tiles alone give fewer than
-// 128 x (CTAs per SM) CTAs; the plan depends on the shapes only (not on the
-// device), so the workspace size is a pure function of them.
+// kTcPlanSms x (CTAs per SM) CTAs; the plan depends on the shapes only (not
+// on the device), so the workspace size is a pure function of them.  The
+// SM count it plans for is the GB300's: the splits fill all 152 SMs (with
+// 128, the long prefill's 32 tiles took eight splits and left 24 SMs idle).
+constexpr int64_t kTcPlanSms = 152;
 ReplayTcPlan replay_tc_plan(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_t Dv) {
     ReplayTcPlan p{};
     p.bytes = -1;
@@ -47,7 +50,7 @@ ReplayTcPlan replay_tc_plan(int64_t B, int64_t T, int64_t Hv, int64_t Dk, int64_
     int64_t items = 0, nkb = (T + kTcSteps - 1) / kTcSteps;
     if (__builtin_mul_overflow(B, Hv, &items) || __builtin_mul_overflow(items, p.row_blocks, &items))
         return p;
-    const int64_t want = 128 * (int64_t)tc_ctas_per_sm((int)Dk);
+    const int64_t want = kTcPlanSms * (int64_t)tc_ctas_per_sm((int)Dk);
     int64_t splits = items >= want ? 1 : std::min<int64_t>(nkb, want / items);
     if (splits < 1) splits = 1;
     p.split_steps = ((nkb + splits - 1) / splits) * kTcSteps;

@@ -155,11 +155,12 @@ def creplay(lib, **kw):
 
 def test_chunk_replay_workspace_size(lib):
     # decay weights [B,Hv,T] + totals [B,Hv] (16-byte padded) + partial sums
-    # when the steps are split (fewer than 256 CTAs from the tiles alone at
-    # Dk <= 128, where two CTAs share an SM; 128 above)
+    # when the steps are split (fewer than 304 CTAs from the tiles alone at
+    # Dk <= 128, where two CTAs share each of the 152 SMs; 152 above): 32
+    # tiles of 4096 steps take 9 splits of 464 steps at Dk = 128, 4 at 256
     B, T, Hv, Dk, Dv = 1, 4096, 32, 128, 128
     w, gam = 32 * 4096 * 4, 32 * 4
-    assert lib.gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv) == w + gam + 8 * 32 * 128 * 128 * 4
+    assert lib.gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv) == w + gam + 9 * 32 * 128 * 128 * 4
     assert lib.gdn_chunk_replay_workspace_size(B, T, Hv, 256, Dv) == w + gam + 4 * 32 * 128 * 256 * 4
     assert lib.gdn_chunk_replay_workspace_size(128, 16, 32, 128, 128) == 128 * 32 * 16 * 4 + 128 * 32 * 4
     assert lib.gdn_chunk_replay_workspace_size(0, 16, 32, 128, 128) == 0
