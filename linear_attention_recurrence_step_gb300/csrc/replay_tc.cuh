@@ -329,9 +329,10 @@ __global__ void __launch_bounds__(kTcThreads, tc_ctas_per_sm(DK)) replay_tc_kern
     // warp w fills core matrices cm = w + 8 j: step quad w % 4, row / column
     // group 2 j + w / 4 -- one step per lane per stage
     const int kq = warp & 3, gq = warp >> 2;
-    // the decay weight of this lane's step, loaded four stages ahead (a
-    // global load the fill depends on: issued in its own stage it would stall
-    // every stage for a DRAM round trip)
+    // the decay weight of this lane's step, from a register ring filled four
+    // stages ahead (a global load the fill depends on: issued in its own
+    // stage it would stall every stage for a round trip; the ring's register
+    // moves still tie each load to the stage after the one that issued it)
     auto weight_of = [&](int s) {
         const int64_t t = t_begin + (int64_t)s * KB + 4 * kq + cs;
         return s < nstages && t < t_end ? wn[t] : 0.f;
