@@ -304,21 +304,29 @@ chunk_local_kernel(const ChunkArgs a) {
             if (a.g_log && on) static_cast<TIn *>(a.g_log)[gi] = gr;
         }
         __syncthreads();  // g, beta of these heads; Gram entries (first pass)
-        for (int e = tid; e < nh * C * C; e += kCkLocalThreads) {
-            const int i = e / (C * C), t = (e >> 4) & 15, u = e & 15;
-            const float *gh = sg + i * C;
-            float p = 1.f;
-            for (int x = u + 1; x <= t; ++x) p *= gh[x];
-            sA[(i * C + t) * CS + u] = u <= t ? p : 0.f;
-            sN[(i * C + t) * CS + u] = u < t ? sb[i * C + t] * p * KK(t, u) : 0.f;
-            if (u == 0) {
-                float Gm = 1.f;
-                for (int x = 0; x <= t; ++x) Gm *= gh[x];
-                sG[i * C + t] = Gm;
+        if (tid < nh * C) {
+            // column u of head i, walked down the steps: A[t][u] = A[t-1][u] g_t
+            // from A[u][u] = 1 (the products in the same order as a walk from
+            // g_{u+1} to g_t), N below the diagonal, Gam_t = g_0 ... g_t
+            const int i = tid / C, u = tid - i * C;
+            const float *gh = sg + i * C, *bh = sb + i * C;
+            float p = 1.f, gm = 1.f;
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                const float gt = gh[t];
+                if (t > u) p *= gt;
+                sA[(i * C + t) * CS + u] = t >= u ? p : 0.f;
+                sN[(i * C + t) * CS + u] = t > u ? bh[t] * p * KK(t, u) : 0.f;
+                gm *= gt;
+                if (u == 0) sG[i * C + t] = gm;
             }
         }
         __syncthreads();
 
+        // workspace block of the pass's head i: a base for (b, chunk) and a
+        // stride per value head
+        float *const ws_b = a.workspace + (b * a.Hv * nch + c) * kCkWsFloats;
+        auto ws_of = [&](int i) { return ws_b + hv_of(i) * (nch * kCkWsFloats); };
         if (tid < nh * C) {
             // W = (I + N)^-1 of head i, one column u per thread, held in registers:
             // W[t][u] = -sum_{x < t} N[t][x] W[x][u]  (W[x][u] = 0 for x < u)
@@ -333,7 +341,7 @@ chunk_local_kernel(const ChunkArgs a) {
                 w[t] = t < u ? 0.f : (t == u ? 1.f : -acc);
             }
             const float bu = sb[i * C + u];
-            float *ws = a.workspace + ((b * a.Hv + hv_of(i)) * nch + c) * kCkWsFloats;
+            float *ws = ws_of(i);
 #pragma unroll
             for (int t = 0; t < C; ++t) ws[t * C + u] = w[t] * bu;  // Wb
         }
@@ -342,12 +350,12 @@ chunk_local_kernel(const ChunkArgs a) {
             const int nf = kCkLocalThreads - nh * C;
             for (int e = ft; e < nh * C * C; e += nf) {
                 const int i = e / (C * C), j = e - i * C * C, t = j >> 4, u = j & 15;
-                float *ws = a.workspace + ((b * a.Hv + hv_of(i)) * nch + c) * kCkWsFloats;
+                float *ws = ws_of(i);
                 ws[C * C + j] = u <= t ? sA[(i * C + t) * CS + u] * KQ(t, u) : 0.f;  // Mq
             }
             for (int e = ft; e < nh * 2 * C; e += nf) {
                 const int i = e / (2 * C), j = e - i * 2 * C;
-                float *ws = a.workspace + ((b * a.Hv + hv_of(i)) * nch + c) * kCkWsFloats;
+                float *ws = ws_of(i);
                 ws[2 * C * C + j] = j < C ? sG[i * C + j] : sA[(i * C + C - 1) * CS + (j - C)];  // Gam, aC
             }
         }
