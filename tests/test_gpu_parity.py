@@ -601,8 +601,8 @@ def test_chunk_replay_tape_beyond_register_cache(dev, T, accepted):
     """One head with a long tape: the decay-weights kernel keeps up to 8192
     steps per tile in registers (eight per thread), so T = 8192 is its last
     cached length and T = 9000 walks the steps and loads them again for the
-    suffix pass; the steps split over well over eight CTAs, so the reduce
-    adds partials past its first batch of eight."""
+    suffix pass; the steps split over some 250-280 CTAs, so the reduce adds
+    partials well past its first batch of eight."""
     case = workloads.make_case(B=1, T=T, Hk=1, Hv=1, Dk=64, Dv=32, dtype="f32", seed=911 + T,
                                g_range=(0.999, 1.0), mask="bernoulli:0.9", accepted=accepted)
     ref = oracle.record(*_oracle_inputs(case))
