@@ -456,6 +456,19 @@ def test_chunk_prefill(dev, spec):
     _check_record(case, got, ref)
 
 
+@pytest.mark.parametrize("gqa", ["block", "tiled"])
+def test_chunk_prefill_more_value_heads_than_a_pass(dev, gqa):
+    """Six value heads per key head: the chunk-local kernel handles four
+    heads per pass, so its second pass (two heads, their g / beta loaded in
+    the pass, their workspace blocks past the first four) runs too; both
+    head mappings, masked steps, tape capture."""
+    case = workloads.make_case(B=2, T=40, Hk=2, Hv=12, Dk=64, Dv=24, dtype="f32", seed=713,
+                               mask="bernoulli:0.8")
+    got, s0, mask = _run_chunk(case, dev, gqa=gqa)
+    ref = oracle.record(*_oracle_inputs(case), gqa=gqa)
+    _check_record(case, got, ref)
+
+
 def test_chunk_prefill_long_tiled(dev):
     """The long-prefill workload (T = 4096, f32, 16 key heads read in place
     by 32 value heads with the tiled mapping) against the oracle."""
