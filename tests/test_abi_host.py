@@ -166,6 +166,25 @@ def test_chunk_replay_workspace_size(lib):
     assert lib.gdn_chunk_replay_workspace_size(0, 16, 32, 128, 128) == 0
 
 
+@pytest.mark.parametrize("B,Hv,T,Dk,splits", [
+    (1, 32, 4096, 128, 9),    # 32 tiles: 304 // 32 = 9 splits of 464 steps (288 CTAs)
+    (1, 100, 4096, 128, 3),   # 100 tiles: 3 splits (300 CTAs)
+    (2, 152, 4096, 128, 1),   # 304 tiles fill the GPU alone: no split, no partial sums
+    (1, 32, 4096, 256, 4),    # Dk = 256, one CTA per SM: 152 // 32 = 4 splits
+    (1, 1, 100, 128, 7),      # a short tape splits no finer than its 16-step stages
+])
+def test_chunk_replay_split_plan(lib, B, Hv, T, Dk, splits):
+    """The tensor-core replay splits the steps of each tile over CTAs until
+    the tiles fill 152 SMs (two CTAs each up to Dk = 128, one above), in
+    whole 16-step stages; the partial sums of the splits are the workspace
+    beyond the decay weights and totals."""
+    Dv = 128
+    w = -(-B * Hv * T * 4 // 16) * 16
+    gam = -(-B * Hv * 4 // 16) * 16
+    part = 0 if splits == 1 else splits * B * Hv * Dv * Dk * 4
+    assert lib.gdn_chunk_replay_workspace_size(B, T, Hv, Dk, Dv) == w + gam + part
+
+
 CREPLAY_CASES = {
     "null workspace": (dict(workspace=None), INVALID),
     "workspace too small": (dict(workspace_bytes=16), INVALID),
